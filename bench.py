@@ -1,0 +1,341 @@
+"""Benchmark: GPTQ layer solve on one 7B attention projection per GPU.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (per GPU): W bf16 4096 x 4096 ~ N(0, 0.02^2); calibration X fp16
+4096 x 262144 (128 sequences x 2048 tokens) ~ N(0, 1) with 1% of channels
+scaled by U[10, 50]; 4-bit asymmetric, group 128, damp 0.01, blocksize 128,
+desc_act off.  A step is one pass of the whole solver on that layer:
+S = 0; S += X X^T; prepare H^-1 factor; quantize; pack.  The inputs are
+resident in HBM when the timed region starts; X (2.15 GB) is larger than
+L2, so no extra flush is needed.
+
+Prints one JSON line (rank 0).  Metric: weights quantized per second
+(Mweights/s), whole job.  With torchrun (N > 1) every rank solves its own
+layer (weak scaling, no collective on the data path); the time is the max
+over ranks.
+
+--impl reference times the CPU oracle (the same algorithm in NumPy fp64) on
+a bounded sample of the same workload and extrapolates to the full layer.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D = 4096
+N_TOK = 262144
+METRIC = "GPTQ layer-solve Mweights/s (4096x4096, 4-bit g128)"
+WORKLOAD = ("7B attention projection: W bf16 4096x4096 N(0,0.02^2); X fp16 4096x262144 "
+            "N(0,1), 1% channels x U[10,50]; 4-bit asym g128, damp 0.01, blocksize 128, "
+            "desc_act off")
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self) -> dict:
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), active=parts[4],
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- inputs
+def make_inputs():
+    from post_weight_quantization_31_b300 import workloads as wl
+    return wl.attn_proj_7b(seed=1002, n_tok=N_TOK, d=D)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib
+
+    build_lib.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp = make_inputs()
+    cfg = inp.cfg
+    X = torch.from_numpy(inp.X).to(dev)
+    W = torch.from_numpy(inp.W).to(torch.bfloat16).to(dev)
+    solver = api.LayerSolver(D, D, cfg, device=dev, exact_diag=False)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        solver.reset()
+        if ev is not None:
+            ev[0].record(stream)
+        solver.accumulate(X)
+        if ev is not None:
+            ev[1].record(stream)
+        solver.prepare()
+        if ev is not None:
+            ev[2].record(stream)
+        solver.quantize(W)
+        if ev is not None:
+            ev[3].record(stream)
+        solver.pack()
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = api.launch_count()
+    with ClockSampler(local_rank) as clk:
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    launches = api.launch_count() - n0
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ph = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+          for i, name in enumerate(("hessian", "prepare", "quantize", "pack"))}
+
+    # end to end through the public host-buffer API
+    e2e = None
+    if args.e2e_steps > 0:
+        chunk = 32768
+        chunks = [torch.from_numpy(np.ascontiguousarray(inp.X[:, a:a + chunk])).pin_memory()
+                  for a in range(0, N_TOK, chunk)]
+        W_host = torch.from_numpy(inp.W).to(torch.bfloat16).pin_memory()
+        api.quantize_layer_from_host(W_host, chunks, cfg, solver=solver)  # warm
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            res = api.quantize_layer_from_host(W_host, chunks, cfg, solver=solver)
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        h2d = sum(c.numel() * c.element_size() for c in chunks) + W_host.numel() * 2
+        d2h = sum(v.numel() * v.element_size() for v in res.values())
+        e2e = {"value": round(world * D * D * args.e2e_steps / e2e_s / 1e6, 3),
+               "unit": "Mweights/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    peaks = measured_peaks()
+    syrk_ms = ph["hessian"]
+    flops = float(N_TOK) * D * (D + 1)       # symmetric half of X X^T
+    achieved = flops / (syrk_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", 1400.0))
+    roof = {"kernel": "hessian_syrk_kernel (tcgen05 kind::f16, fp16 x fp16 -> fp32)",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_note": f"{peaks['source']} bf16 dense sustained (fp16 rate = bf16 rate)",
+            "traffic": args.syrk_traffic}
+    ms_step = elapsed_ms / args.steps
+    line = {
+        "metric": METRIC,
+        "value": round(world * D * D * args.steps / (elapsed_ms * 1e-3) / 1e6, 3),
+        "unit": "Mweights/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 x fp16 -> fp32 (Hessian), fp32 (solve)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "d_row": D, "d_col": D, "n_tok": N_TOK,
+                   "l2": "inputs larger than L2 (X is 2.15 GB)",
+                   "parallelism": f"one independent layer per GPU x{world}"},
+        "phases_ms": {k: round(v, 4) for k, v in ph.items()},
+        "gpu_launches": int(launches),
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, quick=args.quick_cpu)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(inp, quick: bool = False) -> dict:
+    """Times the oracle on a bounded sample and extrapolates to one layer:
+    Hessian on `tok` tokens (scaled by N/tok), the full prepare, the column
+    loop and packing on `rows` rows (scaled by d_row/rows)."""
+    import oracle as O
+    tok = 2048 if quick else 8192
+    rows = 16 if quick else 64
+    t0 = time.perf_counter()
+    S_s = O.hessian_sum(inp.X[:, :tok])
+    t_h = time.perf_counter() - t0
+    S_full = S_s * (N_TOK / tok)      # same scale as the full sum; values of the sample
+    t0 = time.perf_counter()
+    perm, Hp, U = O.prepare(S_full, N_TOK, inp.cfg)
+    t_p = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    Wp = inp.W[:rows].astype(np.float64)[:, perm]
+    codes, scales, zeros, Q = O.column_loop(Wp, U, inp.cfg)
+    t_q = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.pack_qweight(codes, inp.cfg.bits)
+    O.pack_qzeros(zeros, inp.cfg.bits)
+    t_k = time.perf_counter() - t0
+    full_s = t_h * (N_TOK / tok) + t_p + (t_q + t_k) * (D / rows)
+    return {"value": round(D * D / full_s / 1e6, 6), "unit": "Mweights/s",
+            "cores": _blas_threads(), "kind": "oracle",
+            "sample": (f"Hessian on {tok} of {N_TOK} tokens (x{N_TOK // tok}), full prepare "
+                       f"(d=4096), column loop + pack on {rows} of {D} rows (x{D // rows}); "
+                       f"measured {t_h + t_p + t_q + t_k:.1f} s, extrapolated {full_s:.1f} s "
+                       f"per layer"),
+            "seconds_per_layer": round(full_s, 2)}
+
+
+def run_reference(args, rank: int) -> dict | None:
+    if rank != 0:
+        return None
+    inp = make_inputs()
+    vals = []
+    base = None
+    if args.warmup > 0:
+        cpu_baseline(inp, quick=True)
+    for _ in range(args.steps):
+        base = cpu_baseline(inp, quick=args.quick_cpu)
+        vals.append(base["value"])
+    v = statistics.median(vals)
+    ms = D * D / (v * 1e6) * 1e3
+    return {"metric": METRIC, "value": v, "unit": "Mweights/s", "impl": "reference",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "d_row": D, "d_col": D, "n_tok": N_TOK},
+            "cpu_baseline": {"value": v, "unit": "Mweights/s", "cores": base["cores"],
+                             "kind": "oracle", "sample": base["sample"]},
+            "e2e": {"value": v, "unit": "Mweights/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
+    ap.add_argument("--syrk-traffic", type=float, default=None,
+                    help="DRAM bytes per Hessian launch from an ncu capture")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if args.warmup < 3:
+            print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

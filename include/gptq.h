@@ -1,0 +1,227 @@
+/*
+ * gptq.h -- C ABI of the GPTQ per-layer weight-quantization solver for
+ * NVIDIA B300 (sm_103a).
+ *
+ * The solver quantizes one linear layer W [d_row, d_col] (out_features x
+ * in_features) to bits-wide integer codes with one scale and zero point per
+ * group of input columns, using the layer's calibration activations
+ * X [d_col, n_tok].  It is split into four calls that run back to back on
+ * one CUDA stream:
+ *
+ *   gptq_hessian_accumulate   S += X X^T                          (step a1)
+ *   gptq_prepare_hinv         H = 2/n S + damping, column order,
+ *                             U with H^-1 = U^T U                  (step a2)
+ *   gptq_quantize_layer       column loop with error feedback and
+ *                             128-column lazy batch updates        (a3, a4)
+ *   gptq_pack                 codes -> int32 words                 (step a5)
+ *
+ * Sources for what each step computes (web pages on GPTQ):
+ *   [G] GPTQ practical guide, m.lqnn.cn/news/117696: §2.1 "从OBQ说起"
+ *       (OBQ update, Hessian from calibration activations), §2.2 "固定顺序、
+ *       Lazy Batch、Cholesky", §3.3 "量化超参怎么设置" (bits, group_size,
+ *       desc_act, damp_percent), §3.4 (saving the packed model), §5.2
+ *       (desc_act column re-order at load time).
+ *   [S] "AWQ与GPTQ谁更强？ms-swift量化模块深度评测", GPTQ section
+ *       (GptqConfig with sym=True).
+ *   [E] "大模型压缩量化技术：GPTQ 与 AWQ 原理详解 + Python 实战教程", §二
+ *       (min-max round-to-nearest grid), FAQ Q6 (group_size = -1).
+ *
+ * Conventions for every call:
+ *   - All array arguments are DEVICE pointers (memory the caller allocated
+ *     on the current CUDA device), unless the comment says "host".  The
+ *     library never allocates device memory; scratch space is queried with
+ *     the *_workspace_size functions and passed in by the caller.
+ *   - Matrices are row-major and densely packed unless a leading dimension
+ *     is given.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  gptq_prepare_hinv and gptq_quantize_layer synchronize the
+ *     stream once at their end to read back a device status word; the other
+ *     calls are asynchronous.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and return GPTQ_ERR_INVALID_ARG (or GPTQ_ERR_WORKSPACE) with no side
+ *     effect.  A CUDA error at launch returns GPTQ_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded in time (about 2 s).  A wait that
+ *     runs out sets a sticky fault flag on the device and the kernel returns
+ *     early; the next gptq_prepare_hinv / gptq_quantize_layer /
+ *     gptq_device_fault call reports GPTQ_ERR_TIMEOUT and clears it.
+ *   - Only one device is used per call: the current device of the calling
+ *     host thread.
+ */
+#ifndef GPTQ_B300_H
+#define GPTQ_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GPTQ_API __attribute__((visibility("default")))
+#else
+#define GPTQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* gptq_stream_t;
+
+/*
+ * Quantizer knobs, mirroring BaseQuantizeConfig / GptqConfig on the pages
+ * ([G] §3.3, [S]).
+ *   bits          2, 3, 4 or 8.
+ *   group_size    columns sharing one scale and zero point, counted in
+ *                 processing order: a multiple of 32 that divides both
+ *                 d_col and blocksize; or -1 for one group per row
+ *                 ([E] FAQ Q6).
+ *   damp_percent  >= 0; lambda = damp_percent * mean(diag H) is added to
+ *                 diag(H) ([G] §3.3, "防止矩阵奇异").
+ *   blocksize     lazy-batch width ([G] §2.2); must be 128.
+ *   desc_act      0: natural column order; 1: descending diag(H), stable.
+ *   sym           0: asymmetric grid over [min(0,min w), max(0,max w)];
+ *                 1: symmetric grid, scale 2*max|w|/maxq, zero (maxq+1)/2.
+ */
+typedef struct {
+  int32_t bits;
+  int32_t group_size;
+  float damp_percent;
+  int32_t blocksize;
+  int32_t desc_act;
+  int32_t sym;
+} gptq_config_t;
+
+typedef enum {
+  GPTQ_OK = 0,
+  GPTQ_ERR_INVALID_ARG = 1, /* bad size, knob, alignment or null pointer */
+  GPTQ_ERR_NOT_PD = 2,      /* damped H has a non-positive pivot: retry with a
+                               larger damp_percent (the pages' remedy, [G]
+                               §3.3 and the 0.1 damping advice) */
+  GPTQ_ERR_NONFINITE = 3,   /* NaN or Inf in S or W */
+  GPTQ_ERR_WORKSPACE = 4,   /* workspace pointer null or too small */
+  GPTQ_ERR_TIMEOUT = 5,     /* a bounded wait inside a kernel ran out */
+  GPTQ_ERR_CUDA = 6,        /* CUDA runtime error (launch, copy, device) */
+  GPTQ_ERR_UNSUPPORTED = 7  /* device is not sm_103 */
+} gptq_status_t;
+
+/* Storage type of W given to gptq_quantize_layer. */
+enum { GPTQ_W_FP32 = 0, GPTQ_W_BF16 = 1, GPTQ_W_FP16 = 2 };
+
+/*
+ * a1  S += X X^T   ([G] §2.1: the Hessian is computed from the layer's
+ *                   calibration activations; H = 2/n S is formed in a2.)
+ *   X       fp16 [d_col, n_tok] with row stride ldx elements (tokens
+ *           contiguous).  16-byte aligned, ldx >= n_tok, ldx % 8 == 0.
+ *           Read only.
+ *   S       fp32 [d_col, d_col], row-major, 16-byte aligned, updated in place
+ *           with the full symmetric product (both triangles).  Zero it
+ *           before the first call; call once per chunk of tokens.
+ *   diag    fp64 [d_col] or NULL: if given, diag[i] += sum_t X[i,t]^2 computed
+ *           to about 1e-14 relative (double-float sums on the fp32 ALUs).
+ *           gptq_prepare_hinv takes the act-order (desc_act) column order
+ *           from it, so that near-equal diagonals are ordered as exact
+ *           arithmetic orders them; an fp32 diagonal would reorder them.
+ *           Zero it with S.  Costs one extra read of X.
+ *   n_seen  HOST pointer, may be NULL: *n_seen += n_tok on success.
+ *   d_col % 32 == 0, d_col >= 32, n_tok >= 1.
+ *   S runs on the 5th-generation tensor cores (fp16 x fp16 -> fp32).  The
+ *   fp32 sums are added with atomics, so the order of additions, and hence
+ *   the last bits of S, can differ from run to run.  Asynchronous.
+ */
+GPTQ_API gptq_status_t gptq_hessian_accumulate(const void* X, int64_t d_col, int64_t n_tok,
+                                      int64_t ldx, float* S, double* diag, int64_t* n_seen,
+                                      gptq_stream_t stream);
+
+/* Bytes of workspace gptq_prepare_hinv needs for d_col. */
+GPTQ_API size_t gptq_prepare_workspace_size(int64_t d_col);
+
+/*
+ * a2  From S and the token count n_seen: H = (2/n_seen) S;
+ *     H += damp_percent * mean(diag H) * I; if desc_act, perm = stable
+ *     argsort of -diag(H) ([G] §2.2 fixed order, §3.3 desc_act), else the
+ *     identity; then U, upper triangular with positive diagonal, such that
+ *     H[perm][:,perm]^-1 = U^T U ([G] §2.2 Cholesky reformulation).
+ *   S       fp32 [d_col, d_col] from gptq_hessian_accumulate; only the lower
+ *           triangle (i >= j) is read.  Read only.
+ *   diag    fp64 [d_col] from gptq_hessian_accumulate, or NULL.  Used for the
+ *           damping mean and the desc_act order when given; otherwise the
+ *           fp32 diagonal of S is used.
+ *   U       fp32 [d_col, d_col] output, rows and columns in processing
+ *           order; entries below the diagonal are written as 0.
+ *   perm    int32 [d_col] output: perm[i] = original column processed i-th.
+ *   ws      workspace of at least gptq_prepare_workspace_size(d_col) bytes,
+ *           256-byte aligned.
+ *   Returns GPTQ_ERR_NOT_PD for a non-positive pivot (U is then undefined),
+ *   GPTQ_ERR_NONFINITE for NaN/Inf in S.  Synchronizes `stream`.
+ */
+GPTQ_API gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
+                                const gptq_config_t* cfg, float* U, int32_t* perm,
+                                void* ws, size_t ws_bytes, gptq_stream_t stream);
+
+/* Bytes of workspace gptq_quantize_layer needs. */
+GPTQ_API size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const gptq_config_t* cfg);
+
+/*
+ * a3 + a4  Quantize W column by column in processing order with OBQ error
+ *     feedback ([G] §2.1; update w_F -= (w_j - dq_j)/U_jj * U[j, F]) and
+ *     128-column lazy batches ([G] §2.2; after each block,
+ *     W[:, i2:] -= Err U[i1:i2, i2:]).  At the first column of each group the
+ *     group's scale and zero point are set from the group's current,
+ *     error-updated values.  Codes are decided in fp32:
+ *     code = clamp(rint(w * (1/s)) + z, 0, 2^bits - 1).
+ *   W       [d_row, d_col] of type w_dtype (GPTQ_W_FP32/BF16/FP16), 16-byte
+ *           aligned.  Read only (the fp32 working copy lives in ws).
+ *   U, perm outputs of gptq_prepare_hinv for the same cfg.
+ *   codes   uint8 [d_row, d_col] output, ORIGINAL column order.
+ *   scales  fp32  [G, d_row] output, G = d_col/group_size (1 if -1); group
+ *           g covers processing positions [g*gs, (g+1)*gs).
+ *   zeros   uint8 [G, d_row] output.
+ *   g_idx   int32 [d_col] output: group of each original column.
+ *   ws      workspace of gptq_quantize_workspace_size bytes, 256-byte aligned.
+ *   d_row % 32 == 0, d_col % 32 == 0.  Returns GPTQ_ERR_NONFINITE for NaN/Inf
+ *   in W.  Synchronizes `stream`.
+ */
+GPTQ_API gptq_status_t gptq_quantize_layer(const void* W, int32_t w_dtype, int64_t d_row,
+                                  int64_t d_col, const float* U, const int32_t* perm,
+                                  const gptq_config_t* cfg, uint8_t* codes, float* scales,
+                                  uint8_t* zeros, int32_t* g_idx, void* ws, size_t ws_bytes,
+                                  gptq_stream_t stream);
+
+/*
+ * a5  Pack codes and zero points into int32 words.  The pages only say the
+ *     result is saved in "GPTQ format" with safetensors ([G] §3.4); this
+ *     layout is the library's own:
+ *   qweight int32 [d_col*bits/32, d_row]: column r holds row r's codes as an
+ *           LSB-first bit stream along the input dimension (word k of row r
+ *           holds columns [k*32/bits, (k+1)*32/bits) for bits 2, 4, 8; for
+ *           bits 3, words 3m..3m+2 hold columns [32m, 32m+32) as one stream).
+ *   qzeros  int32 [G, d_row*bits/32]: row g is zeros[g, :] as an LSB-first
+ *           stream along d_row.
+ *   codes / zeros values are masked to `bits` bits.  d_row % 32 == 0,
+ *   d_col % 32 == 0.  Asynchronous.
+ */
+GPTQ_API gptq_status_t gptq_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row,
+                        int64_t d_col, int32_t bits, int32_t group_size, int32_t* qweight,
+                        int32_t* qzeros, gptq_stream_t stream);
+
+/* Inverse of gptq_pack (same layouts).  Asynchronous. */
+GPTQ_API gptq_status_t gptq_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row,
+                          int64_t d_col, int32_t bits, int32_t group_size, uint8_t* codes,
+                          uint8_t* zeros, gptq_stream_t stream);
+
+/* Static English text for a status code. */
+GPTQ_API const char* gptq_status_string(gptq_status_t status);
+
+/* Synchronizes `stream`; returns GPTQ_ERR_TIMEOUT (and clears the flag) if a
+ * bounded wait ran out in any kernel of this library since the last check,
+ * else GPTQ_OK (or GPTQ_ERR_CUDA). */
+GPTQ_API gptq_status_t gptq_device_fault(gptq_stream_t stream);
+
+/* Number of kernels this library has launched in this process (all
+ * devices); for instrumentation. */
+GPTQ_API uint64_t gptq_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPTQ_B300_H */

@@ -1,0 +1,313 @@
+"""Python API over the C ABI: the same four calls, taking torch tensors.
+
+PyTorch only provides device memory and the current CUDA stream; every step
+of the solver runs in libgptq_b300.so.  All tensors must live on the current
+CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from . import _lib
+from .workloads import QuantConfig
+
+
+class GPTQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = _lib.load()
+        msg = lib.gptq_status_string(int(code)).decode()
+        super().__init__(f"{where}: {_lib.status_name(code)} ({msg})")
+        self.code = int(code)
+
+
+def _check(code: int, where: str) -> None:
+    if int(code) != _lib.GPTQ_OK:
+        raise GPTQError(code, where)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _need(t: torch.Tensor, dtype, name: str, shape=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _contig(t: torch.Tensor, name: str) -> None:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def n_groups(group_size: int, d_col: int) -> int:
+    return 1 if group_size == -1 else d_col // group_size
+
+
+def launch_count() -> int:
+    return int(_lib.load().gptq_launch_count())
+
+
+# ----------------------------------------------------------------------- a1
+def hessian_accumulate(X: torch.Tensor, S: torch.Tensor, diag: torch.Tensor | None = None) -> int:
+    """S += X X^T (and diag += sum_t X^2 in fp64 if given).  X: fp16
+    [d_col, n_tok] with unit stride along tokens.  Returns n_tok."""
+    lib = _lib.load()
+    _need(X, torch.float16, "X")
+    if X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be 2-D with tokens contiguous")
+    d_col, n_tok = X.shape
+    _need(S, torch.float32, "S", (d_col, d_col))
+    _contig(S, "S")
+    if diag is not None:
+        _need(diag, torch.float64, "diag", (d_col,))
+    n = ctypes.c_int64(0)
+    _check(lib.gptq_hessian_accumulate(X.data_ptr(), d_col, n_tok, X.stride(0), S.data_ptr(),
+                                       _ptr(diag), ctypes.byref(n), _stream()),
+           "gptq_hessian_accumulate")
+    return int(n.value)
+
+
+# ----------------------------------------------------------------------- a2
+def prepare_workspace_size(d_col: int) -> int:
+    return int(_lib.load().gptq_prepare_workspace_size(d_col))
+
+
+def prepare_hinv(S: torch.Tensor, n_seen: int, cfg: QuantConfig, diag: torch.Tensor | None = None,
+                 U: torch.Tensor | None = None, perm: torch.Tensor | None = None,
+                 ws: torch.Tensor | None = None):
+    """Returns (U, perm): U fp32 [d, d] upper with H_perm^-1 = U^T U."""
+    lib = _lib.load()
+    d = S.shape[0]
+    _need(S, torch.float32, "S", (d, d))
+    dev = S.device
+    U = torch.empty((d, d), dtype=torch.float32, device=dev) if U is None else U
+    perm = torch.empty(d, dtype=torch.int32, device=dev) if perm is None else perm
+    need = prepare_workspace_size(d)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    c = _lib.make_config(cfg)
+    _check(lib.gptq_prepare_hinv(S.data_ptr(), _ptr(diag), d, int(n_seen), ctypes.byref(c),
+                                 U.data_ptr(), perm.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream()), "gptq_prepare_hinv")
+    return U, perm
+
+
+# ----------------------------------------------------------------------- a3/a4
+def quantize_workspace_size(d_row: int, d_col: int, cfg: QuantConfig) -> int:
+    c = _lib.make_config(cfg)
+    return int(_lib.load().gptq_quantize_workspace_size(d_row, d_col, ctypes.byref(c)))
+
+
+_WDT = {torch.float32: _lib.W_FP32, torch.bfloat16: _lib.W_BF16, torch.float16: _lib.W_FP16}
+
+
+def quantize_layer(W: torch.Tensor, U: torch.Tensor, perm: torch.Tensor, cfg: QuantConfig,
+                   out: dict | None = None, ws: torch.Tensor | None = None) -> dict:
+    """Returns dict(codes uint8 [d_row, d_col] original order, scales fp32
+    [G, d_row], zeros uint8 [G, d_row], g_idx int32 [d_col])."""
+    lib = _lib.load()
+    if W.dtype not in _WDT:
+        raise ValueError("W must be fp32, bf16 or fp16")
+    _contig(W, "W")
+    d_row, d_col = W.shape
+    dev = W.device
+    G = n_groups(cfg.group_size, d_col)
+    out = {} if out is None else out
+    codes = out.setdefault("codes", torch.empty((d_row, d_col), dtype=torch.uint8, device=dev))
+    scales = out.setdefault("scales", torch.empty((G, d_row), dtype=torch.float32, device=dev))
+    zeros = out.setdefault("zeros", torch.empty((G, d_row), dtype=torch.uint8, device=dev))
+    g_idx = out.setdefault("g_idx", torch.empty(d_col, dtype=torch.int32, device=dev))
+    need = quantize_workspace_size(d_row, d_col, cfg)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    c = _lib.make_config(cfg)
+    _check(lib.gptq_quantize_layer(W.data_ptr(), _WDT[W.dtype], d_row, d_col, U.data_ptr(),
+                                   perm.data_ptr(), ctypes.byref(c), codes.data_ptr(),
+                                   scales.data_ptr(), zeros.data_ptr(), g_idx.data_ptr(),
+                                   ws.data_ptr(), ws.numel(), _stream()), "gptq_quantize_layer")
+    return out
+
+
+# ----------------------------------------------------------------------- a5
+def pack(codes: torch.Tensor, zeros: torch.Tensor, bits: int, group_size: int,
+         qweight: torch.Tensor | None = None, qzeros: torch.Tensor | None = None):
+    lib = _lib.load()
+    d_row, d_col = codes.shape
+    G = n_groups(group_size, d_col)
+    dev = codes.device
+    qweight = (torch.empty((d_col * bits // 32, d_row), dtype=torch.int32, device=dev)
+               if qweight is None else qweight)
+    qzeros = (torch.empty((G, d_row * bits // 32), dtype=torch.int32, device=dev)
+              if qzeros is None else qzeros)
+    _check(lib.gptq_pack(codes.data_ptr(), zeros.data_ptr(), d_row, d_col, bits, group_size,
+                         qweight.data_ptr(), qzeros.data_ptr(), _stream()), "gptq_pack")
+    return qweight, qzeros
+
+
+def unpack(qweight: torch.Tensor, qzeros: torch.Tensor, d_row: int, d_col: int, bits: int,
+           group_size: int):
+    lib = _lib.load()
+    G = n_groups(group_size, d_col)
+    dev = qweight.device
+    codes = torch.empty((d_row, d_col), dtype=torch.uint8, device=dev)
+    zeros = torch.empty((G, d_row), dtype=torch.uint8, device=dev)
+    _check(lib.gptq_unpack(qweight.data_ptr(), qzeros.data_ptr(), d_row, d_col, bits, group_size,
+                           codes.data_ptr(), zeros.data_ptr(), _stream()), "gptq_unpack")
+    return codes, zeros
+
+
+def device_fault() -> None:
+    _check(_lib.load().gptq_device_fault(_stream()), "gptq_device_fault")
+
+
+# ----------------------------------------------------------------------- whole layer
+@dataclasses.dataclass
+class LayerResult:
+    qweight: torch.Tensor
+    qzeros: torch.Tensor
+    scales: torch.Tensor
+    g_idx: torch.Tensor
+    codes: torch.Tensor
+    zeros: torch.Tensor
+    perm: torch.Tensor
+    U: torch.Tensor
+
+
+class LayerSolver:
+    """Owns the device buffers for one layer shape and runs the four calls.
+
+    Buffers are allocated once (through PyTorch) and reused, so repeated
+    solves allocate nothing.
+    """
+
+    def __init__(self, d_row: int, d_col: int, cfg: QuantConfig, device="cuda",
+                 exact_diag: bool | None = None):
+        self.d_row, self.d_col, self.cfg = d_row, d_col, cfg
+        self.device = torch.device(device)
+        dev = self.device
+        self.exact_diag = bool(cfg.desc_act) if exact_diag is None else exact_diag
+        G = n_groups(cfg.group_size, d_col)
+        self.S = torch.zeros((d_col, d_col), dtype=torch.float32, device=dev)
+        self.diag = (torch.zeros(d_col, dtype=torch.float64, device=dev)
+                     if self.exact_diag else None)
+        self.n_seen = 0
+        self.U = torch.empty((d_col, d_col), dtype=torch.float32, device=dev)
+        self.perm = torch.empty(d_col, dtype=torch.int32, device=dev)
+        self.ws_prep = torch.empty(prepare_workspace_size(d_col), dtype=torch.uint8, device=dev)
+        self.ws_quant = torch.empty(quantize_workspace_size(d_row, d_col, cfg), dtype=torch.uint8,
+                                    device=dev)
+        self.out = {
+            "codes": torch.empty((d_row, d_col), dtype=torch.uint8, device=dev),
+            "scales": torch.empty((G, d_row), dtype=torch.float32, device=dev),
+            "zeros": torch.empty((G, d_row), dtype=torch.uint8, device=dev),
+            "g_idx": torch.empty(d_col, dtype=torch.int32, device=dev),
+        }
+        self.qweight = torch.empty((d_col * cfg.bits // 32, d_row), dtype=torch.int32, device=dev)
+        self.qzeros = torch.empty((G, d_row * cfg.bits // 32), dtype=torch.int32, device=dev)
+
+    def staging(self, tokens: int) -> list:
+        """Two device buffers [d_col, tokens] fp16 for chunked host input."""
+        cur = getattr(self, "_stage", None)
+        if cur is None or cur[0].shape[1] < tokens:
+            self._stage = [torch.empty((self.d_col, tokens), dtype=torch.float16,
+                                       device=self.device) for _ in range(2)]
+        return self._stage
+
+    def w_buffer(self, dtype) -> torch.Tensor:
+        cur = getattr(self, "_wbuf", None)
+        if cur is None or cur.dtype != dtype:
+            self._wbuf = torch.empty((self.d_row, self.d_col), dtype=dtype, device=self.device)
+        return self._wbuf
+
+    def reset(self) -> None:
+        self.S.zero_()
+        if self.diag is not None:
+            self.diag.zero_()
+        self.n_seen = 0
+
+    def accumulate(self, X: torch.Tensor) -> None:
+        self.n_seen += hessian_accumulate(X, self.S, self.diag)
+
+    def prepare(self) -> None:
+        prepare_hinv(self.S, self.n_seen, self.cfg, diag=self.diag, U=self.U, perm=self.perm,
+                     ws=self.ws_prep)
+
+    def quantize(self, W: torch.Tensor) -> None:
+        quantize_layer(W, self.U, self.perm, self.cfg, out=self.out, ws=self.ws_quant)
+
+    def pack(self) -> None:
+        pack(self.out["codes"], self.out["zeros"], self.cfg.bits, self.cfg.group_size,
+             qweight=self.qweight, qzeros=self.qzeros)
+
+    def solve(self, W: torch.Tensor, X: torch.Tensor | None = None) -> LayerResult:
+        """Accumulate X (if given), then prepare, quantize and pack."""
+        if X is not None:
+            self.accumulate(X)
+        self.prepare()
+        self.quantize(W)
+        self.pack()
+        return self.result()
+
+    def result(self) -> LayerResult:
+        return LayerResult(qweight=self.qweight, qzeros=self.qzeros, scales=self.out["scales"],
+                           g_idx=self.out["g_idx"], codes=self.out["codes"],
+                           zeros=self.out["zeros"], perm=self.perm, U=self.U)
+
+
+def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
+                             solver: LayerSolver | None = None) -> dict:
+    """End to end from host memory.
+
+    X_chunks: sequence of host fp16 tensors [d_col, t_i] (contiguous; pinned
+    for asynchronous copies), e.g. one per batch of calibration sequences.
+    Chunks are copied to the device on a side stream into two alternating
+    staging buffers, overlapped with the Hessian accumulation of the
+    previous chunk; then the layer is solved and the packed result
+    (qweight, qzeros, scales, g_idx) is returned in host memory.
+    """
+    d_row, d_col = W_host.shape
+    solver = solver or LayerSolver(d_row, d_col, cfg)
+    solver.reset()
+    dev = solver.device
+    compute = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    cap = max(int(c.shape[1]) for c in X_chunks)
+    cap = (cap + 7) // 8 * 8
+    stage = solver.staging(cap)
+    ready = [torch.cuda.Event() for _ in stage]
+    free = [torch.cuda.Event() for _ in stage]
+    W_dev = solver.w_buffer(W_host.dtype)
+    with torch.cuda.stream(copy):
+        W_dev.copy_(W_host, non_blocking=True)
+    w_ready = torch.cuda.Event()
+    w_ready.record(copy)
+    for ci, chunk in enumerate(X_chunks):
+        if chunk.shape[0] != d_col or chunk.dtype != torch.float16:
+            raise ValueError("each X chunk must be fp16 [d_col, t]")
+        b = ci % len(stage)
+        t = int(chunk.shape[1])
+        buf = stage[b][:, :t]
+        with torch.cuda.stream(copy):
+            if ci >= len(stage):
+                copy.wait_event(free[b])
+            buf.copy_(chunk, non_blocking=True)
+            ready[b].record(copy)
+        compute.wait_event(ready[b])
+        solver.accumulate(buf)
+        free[b].record(compute)
+    compute.wait_event(w_ready)
+    solver.prepare()
+    solver.quantize(W_dev)
+    solver.pack()
+    r = solver.result()
+    return {"qweight": r.qweight.to("cpu"), "qzeros": r.qzeros.to("cpu"),
+            "scales": r.scales.to("cpu"), "g_idx": r.g_idx.to("cpu")}

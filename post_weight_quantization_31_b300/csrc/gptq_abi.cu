@@ -1,0 +1,226 @@
+// The C ABI (include/gptq.h): argument checks, workspace sizes, status
+// read-back, and the sticky device fault word.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace gptq {
+
+uint64_t g_launches = 0;
+
+__device__ int g_fault_word = 0;
+
+int* fault_word_ptr() {
+  // One address per device; the symbol lives in this library's module.
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fault_word) == cudaSuccess) cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, float* S,
+                                  cudaStream_t st);
+gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t ldx, double* diag,
+                                cudaStream_t st);
+size_t prep_workspace_bytes(int64_t d);
+gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d, int64_t n_seen, float damp,
+                             bool desc_act, float* U, int32_t* perm, void* ws, cudaStream_t st,
+                             int* status_host);
+size_t quant_workspace_bytes(int64_t d_row, int64_t d_col);
+gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row, int64_t d_col, const float* U,
+                              const int32_t* perm, const gptq_config_t& cfg, uint8_t* codes,
+                              float* scales, uint8_t* zeros, int32_t* g_idx, void* ws,
+                              cudaStream_t st, int* status_host);
+gptq_status_t launch_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,
+                          int bits, int n_groups, int32_t* qweight, int32_t* qzeros, cudaStream_t st);
+gptq_status_t launch_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row, int64_t d_col,
+                            int bits, int n_groups, uint8_t* codes, uint8_t* zeros, cudaStream_t st);
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool bits_ok(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 8; }
+
+bool config_ok(const gptq_config_t* c, int64_t d_col) {
+  if (!c) return false;
+  if (!bits_ok(c->bits)) return false;
+  if (c->blocksize != 128) return false;
+  if (!(c->damp_percent >= 0.f) || !std::isfinite(c->damp_percent)) return false;
+  if (c->desc_act != 0 && c->desc_act != 1) return false;
+  if (c->sym != 0 && c->sym != 1) return false;
+  const int gs = c->group_size;
+  if (gs == -1) return true;
+  if (gs <= 0 || gs % 32 != 0) return false;
+  if (c->blocksize % gs != 0) return false;
+  if (d_col % gs != 0) return false;
+  return true;
+}
+
+bool device_ok() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  return major == 10 && minor == 3;
+}
+
+int n_groups_of(int group_size, int64_t d_col) {
+  return group_size == -1 ? 1 : static_cast<int>(d_col / group_size);
+}
+
+// Reads (and clears) the sticky fault word; synchronizes the stream.
+gptq_status_t finish(cudaStream_t st, int status_word) {
+  int fault = 0;
+  int* fw = fault_word_ptr();
+  if (fw) {
+    if (cudaMemcpyAsync(&fault, fw, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return GPTQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GPTQ_ERR_CUDA;
+    if (fault) {
+      const int zero = 0;
+      cudaMemcpyAsync(fw, &zero, sizeof(int), cudaMemcpyHostToDevice, st);
+      cudaStreamSynchronize(st);
+      return GPTQ_ERR_TIMEOUT;
+    }
+  } else if (cudaStreamSynchronize(st) != cudaSuccess) {
+    return GPTQ_ERR_CUDA;
+  }
+  if (status_word & kStatTimeout) return GPTQ_ERR_TIMEOUT;
+  if (status_word & kStatNonFinite) return GPTQ_ERR_NONFINITE;
+  if (status_word & kStatNotPD) return GPTQ_ERR_NOT_PD;
+  return GPTQ_OK;
+}
+
+}  // namespace
+}  // namespace gptq
+
+using namespace gptq;
+
+extern "C" {
+
+gptq_status_t gptq_hessian_accumulate(const void* X, int64_t d_col, int64_t n_tok, int64_t ldx, float* S,
+                                      double* diag, int64_t* n_seen, gptq_stream_t stream) {
+  if (!X || !S) return GPTQ_ERR_INVALID_ARG;
+  if (d_col < 32 || d_col % 32 != 0 || n_tok < 1 || ldx < n_tok || ldx % 8 != 0)
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_col > 46336 || n_tok > (int64_t(1) << 28)) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(S, 16) || (diag && !aligned(diag, 8))) return GPTQ_ERR_INVALID_ARG;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  gptq_status_t s = launch_hessian_syrk(X, d_col, n_tok, ldx, S, st);
+  if (s != GPTQ_OK) return s;
+  if (diag) {
+    s = launch_diag_sumsq(X, d_col, n_tok, ldx, diag, st);
+    if (s != GPTQ_OK) return s;
+  }
+  if (n_seen) *n_seen += n_tok;
+  return GPTQ_OK;
+}
+
+size_t gptq_prepare_workspace_size(int64_t d_col) {
+  if (d_col <= 0) return 0;
+  return prep_workspace_bytes(d_col);
+}
+
+gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
+                                const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
+                                size_t ws_bytes, gptq_stream_t stream) {
+  if (!S || !U || !perm) return GPTQ_ERR_INVALID_ARG;
+  if (d_col < 32 || d_col % 32 != 0 || d_col > 46336 || n_seen < 1) return GPTQ_ERR_INVALID_ARG;
+  if (!config_ok(cfg, d_col)) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(S, 16) || !aligned(U, 16) || !aligned(perm, 4) || (diag && !aligned(diag, 8)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < prep_workspace_bytes(d_col)) return GPTQ_ERR_WORKSPACE;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int status = 0;
+  gptq_status_t s = launch_prepare(S, diag, d_col, n_seen, cfg->damp_percent, cfg->desc_act != 0, U,
+                                   perm, ws, st, &status);
+  if (s != GPTQ_OK) return s;
+  return finish(st, status);
+}
+
+size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const gptq_config_t* cfg) {
+  (void)cfg;
+  if (d_row <= 0 || d_col <= 0) return 0;
+  return quant_workspace_bytes(d_row, d_col);
+}
+
+gptq_status_t gptq_quantize_layer(const void* W, int32_t w_dtype, int64_t d_row, int64_t d_col,
+                                  const float* U, const int32_t* perm, const gptq_config_t* cfg,
+                                  uint8_t* codes, float* scales, uint8_t* zeros, int32_t* g_idx,
+                                  void* ws, size_t ws_bytes, gptq_stream_t stream) {
+  if (!W || !U || !perm || !codes || !scales || !zeros || !g_idx) return GPTQ_ERR_INVALID_ARG;
+  if (w_dtype != GPTQ_W_FP32 && w_dtype != GPTQ_W_BF16 && w_dtype != GPTQ_W_FP16)
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_row < 32 || d_row % 32 != 0 || d_col < 32 || d_col % 32 != 0) return GPTQ_ERR_INVALID_ARG;
+  if (d_row * d_col > (int64_t(1) << 31) - 1 || d_col > 46336) return GPTQ_ERR_INVALID_ARG;
+  if (!config_ok(cfg, d_col)) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(U, 16) || !aligned(scales, 4)) return GPTQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < quant_workspace_bytes(d_row, d_col))
+    return GPTQ_ERR_WORKSPACE;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int status = 0;
+  gptq_status_t s = launch_quantize(W, w_dtype, d_row, d_col, U, perm, *cfg, codes, scales, zeros,
+                                    g_idx, ws, st, &status);
+  if (s != GPTQ_OK) return s;
+  return finish(st, status);
+}
+
+gptq_status_t gptq_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,
+                        int32_t bits, int32_t group_size, int32_t* qweight, int32_t* qzeros,
+                        gptq_stream_t stream) {
+  if (!codes || !zeros || !qweight || !qzeros) return GPTQ_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || d_row < 32 || d_row % 32 != 0 || d_col < 32 || d_col % 32 != 0)
+    return GPTQ_ERR_INVALID_ARG;
+  if (group_size != -1 && (group_size <= 0 || d_col % group_size != 0)) return GPTQ_ERR_INVALID_ARG;
+  if (d_row * d_col > (int64_t(1) << 31) - 1) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(qweight, 4) || !aligned(qzeros, 4)) return GPTQ_ERR_INVALID_ARG;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  return launch_pack(codes, zeros, d_row, d_col, bits, n_groups_of(group_size, d_col), qweight, qzeros,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status_t gptq_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row, int64_t d_col,
+                          int32_t bits, int32_t group_size, uint8_t* codes, uint8_t* zeros,
+                          gptq_stream_t stream) {
+  if (!codes || !zeros || !qweight || !qzeros) return GPTQ_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || d_row < 32 || d_row % 32 != 0 || d_col < 32 || d_col % 32 != 0)
+    return GPTQ_ERR_INVALID_ARG;
+  if (group_size != -1 && (group_size <= 0 || d_col % group_size != 0)) return GPTQ_ERR_INVALID_ARG;
+  if (d_row * d_col > (int64_t(1) << 31) - 1) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(qweight, 4) || !aligned(qzeros, 4)) return GPTQ_ERR_INVALID_ARG;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  return launch_unpack(qweight, qzeros, d_row, d_col, bits, n_groups_of(group_size, d_col), codes, zeros,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* gptq_status_string(gptq_status_t s) {
+  switch (s) {
+    case GPTQ_OK: return "ok";
+    case GPTQ_ERR_INVALID_ARG: return "invalid argument";
+    case GPTQ_ERR_NOT_PD: return "damped Hessian is not positive definite (raise damp_percent)";
+    case GPTQ_ERR_NONFINITE: return "non-finite value in the input";
+    case GPTQ_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GPTQ_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+    case GPTQ_ERR_CUDA: return "CUDA runtime error";
+    case GPTQ_ERR_UNSUPPORTED: return "device is not sm_103 (B300)";
+  }
+  return "unknown status";
+}
+
+gptq_status_t gptq_device_fault(gptq_stream_t stream) {
+  return finish(reinterpret_cast<cudaStream_t>(stream), 0);
+}
+
+uint64_t gptq_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+}  // extern "C"

@@ -1,0 +1,363 @@
+// Steps a3 + a4: the column loop with OBQ error feedback and the 128-column
+// lazy batch update.
+//
+// [G] GPTQ practical guide (m.lqnn.cn/news/117696):
+//   §2.1 quantizing one weight is compensated on the weights not yet
+//        quantized, in the direction given by the inverse Hessian; through
+//        the Cholesky factor U (H^-1 = U^T U) this is
+//        w_F -= (w_j - quant(w_j)) / U_jj * U[j, F];
+//   §2.2 the columns go in one fixed order and the compensation is batched:
+//        quantize 128 columns, then update all remaining columns with one
+//        matrix multiply;
+//   §3.3 every group_size consecutive columns share one scale and zero point.
+// [S] ms-swift review, GPTQ section: sym=True selects a symmetric grid.
+//
+// Kernels (per layer):
+//   load       W (bf16/fp16/fp32) -> fp32 working copy in processing order,
+//              g_idx, non-finite check
+//   rowparams  group_size = -1 only: one (scale, zero) per row from the
+//              initial row
+//   per 128-column block [i1, i2):
+//     column   row-parallel sequential loop over the block's columns:
+//              4 lanes own one row (32 columns each, in registers), the
+//              block of U sits in shared memory, the pivot column's value is
+//              broadcast with one shuffle per column; group min/max by
+//              shuffles; writes codes (original column order), scales,
+//              zeros, and Err = the scaled errors of the block
+//     trailing W[:, i2:] -= Err U[i1:i2, i2:]  (fp32 FFMA tile GEMM)
+//
+// Code decisions are taken in fp32 exactly as:
+//   s = (xmax - xmin) / maxq,  r = 1 / s,  z = rint(-xmin * r)   (asym)
+//   s = 2 a / maxq, r = 1 / s, z = (maxq + 1) / 2, a = max(-xmin, xmax) (sym)
+//   code = min(max(rint(w * r) + z, 0), maxq)
+// with xmin = min(0, min w), xmax = max(0, max w), and the range [-1, 1]
+// when it is empty.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "sgemm.cuh"
+
+namespace gptq {
+namespace {
+
+constexpr int CB = 128;           // block width (blocksize)
+constexpr int SEG = 36;           // padded 32-column segment of a U row in smem
+constexpr int ROWS_PER_WARP = 8;  // 4 lanes per row
+constexpr int CL_WARPS = 2;
+constexpr int CL_ROWS = CL_WARPS * ROWS_PER_WARP;
+constexpr int CL_THREADS = CL_WARPS * 32;
+
+struct QParams {
+  float s, r, z;
+};
+
+__device__ __forceinline__ QParams grid_params(float xmin, float xmax, float maxq, int sym) {
+  xmin = fminf(xmin, 0.f);
+  xmax = fmaxf(xmax, 0.f);
+  QParams p;
+  if (sym) {
+    float a = fmaxf(-xmin, xmax);
+    if (a == 0.f) a = 1.f;
+    p.s = (2.f * a) / maxq;
+    p.r = 1.f / p.s;
+    p.z = 0.5f * (maxq + 1.f);
+  } else {
+    if (xmin == xmax) {
+      xmin = -1.f;
+      xmax = 1.f;
+    }
+    p.s = (xmax - xmin) / maxq;
+    p.r = 1.f / p.s;
+    p.z = rintf(-xmin * p.r);
+  }
+  return p;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half v) {
+  return __half2float(v);
+}
+
+// Wf[r][i] = W[r][perm[i]]; g_idx[perm[i]] = i / gs.
+template <typename T>
+__global__ void load_w_kernel(const T* __restrict__ W, const int32_t* __restrict__ perm, int d_row,
+                              int d_col, int gs, float* __restrict__ Wf, int32_t* __restrict__ g_idx,
+                              int* __restrict__ status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d_col) return;
+  const int src = perm[i];
+  if (blockIdx.y == 0) g_idx[src] = gs > 0 ? i / gs : 0;
+  int bad = 0;
+  for (int r = blockIdx.y; r < d_row; r += gridDim.y) {
+    const float v = to_f32<T>(W[static_cast<size_t>(r) * d_col + src]);
+    if (!isfinite(v)) bad = 1;
+    Wf[static_cast<size_t>(r) * d_col + i] = v;
+  }
+  if (bad) atomicOr(status, kStatNonFinite);
+}
+
+// group_size = -1: (scale, zero) per row from the initial row.
+__global__ void row_params_kernel(const float* __restrict__ Wf, int d_col, float maxq, int sym,
+                                  float* __restrict__ scales, uint8_t* __restrict__ zeros) {
+  __shared__ float smn[32], smx[32];
+  const int r = blockIdx.x;
+  const float* w = Wf + static_cast<size_t>(r) * d_col;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int i = threadIdx.x; i < d_col; i += blockDim.x) {
+    mn = fminf(mn, w[i]);
+    mx = fmaxf(mx, w[i]);
+  }
+  for (int o = 16; o; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    smn[threadIdx.x >> 5] = mn;
+    smx[threadIdx.x >> 5] = mx;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < static_cast<int>(blockDim.x >> 5); ++k) {
+      mn = fminf(mn, smn[k]);
+      mx = fmaxf(mx, smx[k]);
+    }
+    const QParams p = grid_params(mn, mx, maxq, sym);
+    scales[r] = p.s;
+    zeros[r] = static_cast<uint8_t>(p.z);
+  }
+}
+
+struct ColumnArgs {
+  float* Wf;            // [d_row, d_col] working copy (processing order)
+  int d_row, d_col;
+  int i1, ncols;        // block start and width (multiple of 32, <= CB)
+  const float* U;       // [d_col, d_col]
+  const int32_t* perm;  // processing position -> original column
+  float maxq;
+  int gs, sym;
+  uint8_t* codes;       // [d_row, d_col] original order
+  float* scales;        // [G, d_row]
+  uint8_t* zeros;       // [G, d_row]
+  float* Err;           // [d_row, CB]
+};
+
+__global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) {
+  extern __shared__ float smem[];
+  float* Us = smem;                                  // [CB][4 * SEG]
+  float* inv_d = Us + CB * 4 * SEG;                  // [CB]
+  float* err_s = inv_d + CB;                         // [CL_ROWS][CB + 1]
+  uint8_t* code_s = reinterpret_cast<uint8_t*>(err_s + CL_ROWS * (CB + 1));  // [CL_ROWS][CB]
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int row_local = (tid >> 5) * ROWS_PER_WARP + (lane >> 2);
+  const int sub = lane & 3;
+  const int r = blockIdx.x * CL_ROWS + row_local;
+  const int i1 = a.i1, nc = a.ncols, d = a.d_col;
+
+  // U block, rows/cols [i1, i1 + nc), padded by segment.
+  for (int idx = tid; idx < CB * CB; idx += CL_THREADS) {
+    const int jj = idx / CB, c = idx % CB;
+    float v = 0.f;
+    if (jj < nc && c < nc) v = a.U[static_cast<size_t>(i1 + jj) * d + i1 + c];
+    Us[jj * 4 * SEG + (c >> 5) * SEG + (c & 31)] = v;
+  }
+  for (int jj = tid; jj < CB; jj += CL_THREADS)
+    inv_d[jj] = jj < nc ? 1.f / a.U[static_cast<size_t>(i1 + jj) * d + i1 + jj] : 0.f;
+
+  float w[32];
+  const bool row_ok = r < a.d_row;
+  const float* wrow = a.Wf + static_cast<size_t>(r) * d + i1 + 32 * sub;
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_ok && 32 * sub + k < nc) v = *reinterpret_cast<const float4*>(wrow + k);
+    w[k] = v.x;
+    w[k + 1] = v.y;
+    w[k + 2] = v.z;
+    w[k + 3] = v.w;
+  }
+  QParams p{1.f, 1.f, 0.f};
+  if (a.gs <= 0 && row_ok) {
+    p.s = a.scales[r];
+    p.r = 1.f / p.s;
+    p.z = static_cast<float>(a.zeros[r]);
+  }
+  __syncthreads();
+
+  const int src_base = lane & ~3;
+  for (int sub0 = 0; sub0 < (nc >> 5); ++sub0) {
+    const int seg_start = i1 + 32 * sub0;
+    const bool gstart = a.gs > 0 && (seg_start % a.gs) == 0;
+    const float* urow_base = Us + (32 * sub0) * 4 * SEG + sub * SEG;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      if (k == 0 && gstart) {
+        // Group [seg_start, seg_start + gs): lanes sub0 .. sub0 + gs/32 - 1.
+        float mn = INFINITY, mx = -INFINITY;
+        if (sub >= sub0 && sub < sub0 + (a.gs >> 5)) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            mn = fminf(mn, w[t]);
+            mx = fmaxf(mx, w[t]);
+          }
+        }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        p = grid_params(mn, mx, a.maxq, a.sym);
+        if (sub == 0 && row_ok) {
+          const int g = seg_start / a.gs;
+          a.scales[static_cast<size_t>(g) * a.d_row + r] = p.s;
+          a.zeros[static_cast<size_t>(g) * a.d_row + r] = static_cast<uint8_t>(p.z);
+        }
+      }
+      const int j = 32 * sub0 + k;
+      const float v = __shfl_sync(0xffffffffu, w[k], src_base | sub0);
+      const float q = fminf(fmaxf(rintf(v * p.r) + p.z, 0.f), a.maxq);
+      const float dq = p.s * (q - p.z);
+      const float e = (v - dq) * inv_d[j];
+      const float* urow = urow_base + k * 4 * SEG;
+#pragma unroll
+      for (int t = 0; t < 32; t += 4) {
+        const float4 u4 = *reinterpret_cast<const float4*>(urow + t);
+        w[t] = fmaf(-e, u4.x, w[t]);
+        w[t + 1] = fmaf(-e, u4.y, w[t + 1]);
+        w[t + 2] = fmaf(-e, u4.z, w[t + 2]);
+        w[t + 3] = fmaf(-e, u4.w, w[t + 3]);
+      }
+      if (sub == sub0) {
+        err_s[row_local * (CB + 1) + j] = e;
+        code_s[row_local * CB + j] = static_cast<uint8_t>(q);
+      }
+    }
+  }
+  __syncthreads();
+  // Err block and codes (original column order) for this CTA's rows.
+  for (int idx = tid; idx < CL_ROWS * nc; idx += CL_THREADS) {
+    const int rl = idx / nc, c = idx % nc;
+    const int rr = blockIdx.x * CL_ROWS + rl;
+    if (rr >= a.d_row) continue;
+    a.Err[static_cast<size_t>(rr) * CB + c] = err_s[rl * (CB + 1) + c];
+    a.codes[static_cast<size_t>(rr) * d + a.perm[i1 + c]] = code_s[rl * CB + c];
+  }
+}
+
+__global__ void __launch_bounds__(GEMM_THREADS) trailing_kernel(GemmArgs g) {
+  __shared__ GemmSmem s;
+  gemm_tile<false, false, false>(g, blockIdx.y * GM, blockIdx.x * GN, s);
+}
+
+}  // namespace
+
+constexpr size_t kColumnSmem =
+    sizeof(float) * (CB * 4 * SEG + CB + CL_ROWS * (CB + 1)) + CL_ROWS * CB;
+
+struct QuantLayout {
+  size_t status, Wf, Err, total;
+};
+
+static size_t align256q(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static QuantLayout quant_layout(int64_t d_row, int64_t d_col) {
+  QuantLayout L;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.Wf = off;
+  off = align256q(off + sizeof(float) * d_row * d_col);
+  L.Err = off;
+  off = align256q(off + sizeof(float) * d_row * CB);
+  L.total = off;
+  return L;
+}
+
+size_t quant_workspace_bytes(int64_t d_row, int64_t d_col) { return quant_layout(d_row, d_col).total; }
+
+gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64_t d_col64,
+                              const float* U, const int32_t* perm, const gptq_config_t& cfg,
+                              uint8_t* codes, float* scales, uint8_t* zeros, int32_t* g_idx,
+                              void* ws, cudaStream_t st, int* status_host) {
+  const int d_row = static_cast<int>(d_row64), d_col = static_cast<int>(d_col64);
+  const QuantLayout L = quant_layout(d_row64, d_col64);
+  char* base = static_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(base + L.status);
+  float* Wf = reinterpret_cast<float*>(base + L.Wf);
+  float* Err = reinterpret_cast<float*>(base + L.Err);
+  const float maxq = static_cast<float>((1 << cfg.bits) - 1);
+  const int gs = cfg.group_size;
+
+  GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
+  {
+    dim3 grid((d_col + 255) / 256, std::min(d_row, 64));
+    if (w_dtype == GPTQ_W_FP32)
+      load_w_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(W), perm, d_row, d_col, gs,
+                                                 Wf, g_idx, status);
+    else if (w_dtype == GPTQ_W_BF16)
+      load_w_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(W), perm,
+                                                         d_row, d_col, gs, Wf, g_idx, status);
+    else
+      load_w_kernel<__half><<<grid, 256, 0, st>>>(static_cast<const __half*>(W), perm, d_row, d_col,
+                                                  gs, Wf, g_idx, status);
+    GPTQ_LAUNCH_CHECK();
+  }
+  if (gs <= 0) {
+    row_params_kernel<<<d_row, 256, 0, st>>>(Wf, d_col, maxq, cfg.sym, scales, zeros);
+    GPTQ_LAUNCH_CHECK();
+  }
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(column_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(kColumnSmem)));
+  for (int i1 = 0; i1 < d_col; i1 += CB) {
+    const int nc = std::min(CB, d_col - i1);
+    ColumnArgs ca;
+    ca.Wf = Wf;
+    ca.d_row = d_row;
+    ca.d_col = d_col;
+    ca.i1 = i1;
+    ca.ncols = nc;
+    ca.U = U;
+    ca.perm = perm;
+    ca.maxq = maxq;
+    ca.gs = gs;
+    ca.sym = cfg.sym;
+    ca.codes = codes;
+    ca.scales = scales;
+    ca.zeros = zeros;
+    ca.Err = Err;
+    column_block_kernel<<<(d_row + CL_ROWS - 1) / CL_ROWS, CL_THREADS, kColumnSmem, st>>>(ca);
+    GPTQ_LAUNCH_CHECK();
+    const int i2 = i1 + nc;
+    if (i2 < d_col) {
+      GemmArgs g;
+      g.M = d_row;
+      g.N = d_col - i2;
+      g.K = nc;
+      g.alpha = -1.f;
+      g.beta = 1.f;
+      g.A = Err;
+      g.lda = CB;
+      g.B = U + static_cast<int64_t>(i1) * d_col + i2;
+      g.ldb = d_col;
+      g.C = Wf + i2;
+      g.ldc = d_col;
+      trailing_kernel<<<dim3((g.N + GN - 1) / GN, (g.M + GM - 1) / GM), GEMM_THREADS, 0, st>>>(g);
+      GPTQ_LAUNCH_CHECK();
+    }
+  }
+  GPTQ_CUDA_TRY(cudaMemcpyAsync(status_host, status, sizeof(int), cudaMemcpyDeviceToHost, st));
+  return GPTQ_OK;
+}
+
+}  // namespace gptq

@@ -1,0 +1,105 @@
+"""Shared helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (the stated bar for the solver):
+  scales within 1e-5 relative; >= 99.9% of codes identical and none more
+  than 1 level apart; layer reconstruction error ||(W - Q) X||^2 within
+  1e-3 relative; pack/unpack bit-exact.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+import oracle as O
+
+SCALE_RTOL = 1e-5
+CODE_MATCH = 0.999
+RECON_RTOL = 1e-3
+
+
+@dataclasses.dataclass
+class GpuOut:
+    codes: np.ndarray
+    scales: np.ndarray
+    zeros: np.ndarray
+    g_idx: np.ndarray
+    perm: np.ndarray
+    U: np.ndarray
+    S: np.ndarray
+    diag: np.ndarray | None
+    qweight: np.ndarray
+    qzeros: np.ndarray
+    n_seen: int
+
+
+def torch_w(W: np.ndarray, w_dtype: str, device="cuda"):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(W, dtype=np.float32))
+    dt = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}[w_dtype]
+    return t.to(dt).to(device)
+
+
+def gpu_solve(W: np.ndarray, w_dtype: str, X: np.ndarray, cfg, chunks: int = 1,
+              exact_diag: bool | None = None) -> GpuOut:
+    import torch
+    from post_weight_quantization_31_b300 import api
+    d_row, d_col = W.shape
+    Xd = torch.from_numpy(np.ascontiguousarray(X)).cuda()
+    solver = api.LayerSolver(d_row, d_col, cfg, exact_diag=exact_diag)
+    solver.reset()
+    n = X.shape[1]
+    bounds = np.linspace(0, n, chunks + 1).astype(int)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b > a:
+            solver.accumulate(Xd[:, a:b].contiguous())
+    solver.prepare()
+    solver.quantize(torch_w(W, w_dtype))
+    solver.pack()
+    torch.cuda.synchronize()
+    o = solver.out
+    return GpuOut(codes=o["codes"].cpu().numpy().astype(np.int64),
+                  scales=o["scales"].cpu().numpy(), zeros=o["zeros"].cpu().numpy().astype(np.int64),
+                  g_idx=o["g_idx"].cpu().numpy().astype(np.int64),
+                  perm=solver.perm.cpu().numpy().astype(np.int64), U=solver.U.cpu().numpy(),
+                  S=solver.S.cpu().numpy(),
+                  diag=None if solver.diag is None else solver.diag.cpu().numpy(),
+                  qweight=solver.qweight.cpu().numpy(), qzeros=solver.qzeros.cpu().numpy(),
+                  n_seen=solver.n_seen)
+
+
+def compare(g: GpuOut, ref: O.LayerResult, W: np.ndarray, S64: np.ndarray, cfg) -> dict:
+    """Metrics of a GPU result against the oracle's on the same inputs."""
+    same = g.codes == ref.codes
+    Qg = O.dequantize(g.codes, g.scales, g.zeros, g.g_idx)
+    eg, er = O.recon_error(W, Qg, S64), O.recon_error(W, ref.Q, S64)
+    rows_with_flip = int(np.any(~same, axis=1).sum())
+    return dict(
+        code_match=float(same.mean()),
+        code_maxdiff=int(np.abs(g.codes - ref.codes).max()),
+        zero_match=float((g.zeros == ref.zeros).mean()),
+        zero_maxdiff=int(np.abs(g.zeros - ref.zeros).max()),
+        scale_rel=float(np.max(np.abs(g.scales.astype(np.float64) - ref.scales)
+                               / np.abs(ref.scales.astype(np.float64)))),
+        recon_gpu=eg, recon_ref=er, recon_rel=abs(eg - er) / er,
+        rows_with_flip=rows_with_flip,
+        perm_equal=bool(np.array_equal(g.perm, ref.perm)),
+        g_idx_equal=bool(np.array_equal(g.g_idx, ref.g_idx)),
+    )
+
+
+def assert_parity(m: dict, scale_rtol: float = SCALE_RTOL) -> None:
+    assert m["perm_equal"], m
+    assert m["g_idx_equal"], m
+    assert m["code_match"] >= CODE_MATCH, m
+    assert m["code_maxdiff"] <= 1, m
+    assert m["zero_match"] >= CODE_MATCH, m
+    assert m["zero_maxdiff"] <= 1, m
+    assert m["scale_rel"] <= scale_rtol, m
+    assert m["recon_rel"] <= RECON_RTOL, m
+
+
+def s_error(S_gpu: np.ndarray, S64: np.ndarray) -> float:
+    """max |dS_ij| / sqrt(S_ii S_jj)."""
+    dg = np.sqrt(np.maximum(np.diag(S64), 1e-300))
+    return float(np.max(np.abs(S_gpu.astype(np.float64) - S64) / np.outer(dg, dg)))

@@ -1,0 +1,184 @@
+"""GPU path vs the CPU oracle on identical seeded inputs, through the C ABI.
+
+Sizes are ones the oracle finishes in seconds, chosen to span several
+tiles and 128-column blocks and to include ragged tails (d_col not a multiple
+of 128, token counts not a multiple of 64)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from post_weight_quantization_31_b300 import workloads as wl
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from post_weight_quantization_31_b300 import build_lib
+    build_lib.build()
+
+
+def qc(**kw):
+    base = dict(bits=4, group_size=128, damp_percent=0.01, blocksize=128, desc_act=False,
+                sym=False)
+    base.update(kw)
+    return wl.QuantConfig(**base)
+
+
+def run_case(W, w_dtype, X, cfg, chunks=1):
+    g = P.gpu_solve(W, w_dtype, X, cfg, chunks=chunks)
+    S64 = O.hessian_sum(X)
+    ref = O.quantize_layer(W, S64, X.shape[1], cfg)
+    return g, ref, S64, P.compare(g, ref, W, S64, cfg)
+
+
+# ------------------------------------------------------------------ a1
+@pytest.mark.parametrize("d_col,n_tok", [(512, 2048), (544, 2088), (32, 100), (1024, 8192),
+                                         (2048, 777)])
+def test_hessian_matches_exact(d_col, n_tok):
+    import torch
+    from post_weight_quantization_31_b300 import api
+    X = wl.make_activations(d_col, n_tok, seed=d_col + n_tok, n_outliers=3, outlier_scale=20.0)
+    S = torch.zeros((d_col, d_col), dtype=torch.float32, device="cuda")
+    diag = torch.zeros(d_col, dtype=torch.float64, device="cuda")
+    n = api.hessian_accumulate(torch.from_numpy(X).cuda(), S, diag)
+    assert n == n_tok
+    S64 = O.hessian_sum(X)
+    assert P.s_error(S.cpu().numpy(), S64) < 2e-6
+    np.testing.assert_allclose(diag.cpu().numpy(), np.diag(S64), rtol=1e-12)
+
+
+def test_hessian_accumulates_over_chunks_and_strides():
+    import torch
+    from post_weight_quantization_31_b300 import api
+    X = wl.make_activations(256, 3000, seed=5, n_outliers=2, outlier_scale=10.0)
+    Xd = torch.zeros((256, 3008), dtype=torch.float16, device="cuda")  # padded rows (ldx 3008)
+    Xd[:, :3000] = torch.from_numpy(X).cuda()
+    S = torch.zeros((256, 256), dtype=torch.float32, device="cuda")
+    n = 0
+    for a, b in [(0, 1000), (1000, 1004), (1004, 3000)]:
+        n += api.hessian_accumulate(Xd[:, a:b], S)
+    assert n == 3000
+    assert P.s_error(S.cpu().numpy(), O.hessian_sum(X)) < 2e-6
+
+
+# ------------------------------------------------------------------ a2
+@pytest.mark.parametrize("d_col,desc_act", [(512, False), (544, True), (1024, True), (2080, False)])
+def test_prepare_matches_oracle(d_col, desc_act):
+    import torch
+    from post_weight_quantization_31_b300 import api
+    X = wl.make_activations(d_col, 4 * d_col, seed=d_col, outlier_frac=0.01)
+    cfg = qc(desc_act=desc_act, group_size=32)
+    S = torch.zeros((d_col, d_col), dtype=torch.float32, device="cuda")
+    diag = torch.zeros(d_col, dtype=torch.float64, device="cuda")
+    n = api.hessian_accumulate(torch.from_numpy(X).cuda(), S, diag)
+    U, perm = api.prepare_hinv(S, n, cfg, diag=diag)
+    S64 = O.hessian_sum(X)
+    perm_o, Hp, U_o = O.prepare(S64, n, cfg)
+    assert np.array_equal(perm.cpu().numpy(), perm_o)
+    Ug = U.cpu().numpy().astype(np.float64)
+    assert np.all(np.tril(Ug, -1) == 0)
+    assert np.all(np.diag(Ug) > 0)
+    err = np.max(np.abs(Ug - U_o)) / np.max(np.abs(U_o))
+    assert err < 2e-4, err
+    # U^T U H = I with the oracle's H
+    R = Ug.T @ (Ug @ Hp)
+    assert np.max(np.abs(R - np.eye(d_col))) < 5e-3
+
+
+# ------------------------------------------------------------------ a3-a5 end to end
+def test_tiny_layer_parity():
+    inp = wl.tiny_layer()
+    g, ref, S64, m = run_case(inp.W, inp.w_dtype, inp.X, inp.cfg)
+    P.assert_parity(m)
+    assert np.array_equal(g.qweight, O.pack_qweight(g.codes, inp.cfg.bits))
+    assert np.array_equal(g.qzeros, O.pack_qzeros(g.zeros, inp.cfg.bits))
+
+
+CASES = [
+    # (d_row, d_col, n_tok, w_dtype, cfg kwargs)
+    (128, 1024, 4096, "bf16", dict()),
+    (128, 1024, 4096, "bf16", dict(sym=True)),
+    (96, 1024, 4096, "fp16", dict(bits=3, group_size=64, desc_act=True, sym=True,
+                                  damp_percent=0.1)),
+    (96, 1024, 4096, "bf16", dict(bits=2, group_size=64, desc_act=True, sym=True,
+                                  damp_percent=0.1)),
+    (64, 512, 2048, "fp32", dict(bits=8, group_size=32)),
+    (64, 1024, 4096, "bf16", dict(group_size=-1, desc_act=True)),
+    (96, 544, 2088, "bf16", dict(group_size=32)),          # ragged last block and tokens
+    (64, 640, 1500, "fp32", dict(bits=3, group_size=-1, sym=True)),
+]
+
+
+@pytest.mark.parametrize("d_row,d_col,n_tok,w_dtype,kw", CASES)
+def test_layer_parity(d_row, d_col, n_tok, w_dtype, kw):
+    cfg = qc(**kw)
+    X = wl.make_activations(d_col, n_tok, seed=d_col * 7 + n_tok, outlier_frac=0.01)
+    W = wl.make_weight(d_row, d_col, seed=d_row + d_col, dtype="fp32" if w_dtype == "fp32" else "bf16")
+    if w_dtype == "fp16":
+        W = W.astype(np.float16).astype(np.float32)
+    g, ref, S64, m = run_case(W, w_dtype, X, cfg, chunks=2)
+    P.assert_parity(m)
+    assert np.array_equal(g.qweight, O.pack_qweight(g.codes, cfg.bits))
+
+
+def test_replay_isolates_compensation():
+    """Strongly correlated X: free-running codes may cascade apart, so the
+    oracle is replayed with the GPU's codes; scales and the reconstruction
+    error then have to agree."""
+    cfg = qc(group_size=64, desc_act=True)
+    X = wl.make_correlated_activations(512, 2048, seed=77)
+    W = wl.make_weight(64, 512, seed=78, dtype="bf16")
+    g = P.gpu_solve(W, "bf16", X, cfg)
+    S64 = O.hessian_sum(X)
+    free = O.quantize_layer(W, S64, X.shape[1], cfg)
+    rep = O.quantize_layer(W, S64, X.shape[1], cfg, forced_codes=g.codes)
+    assert np.array_equal(g.perm, rep.perm)
+    rel = np.max(np.abs(g.scales.astype(np.float64) - rep.scales) / rep.scales)
+    assert rel <= 1e-4, rel
+    Qg = O.dequantize(g.codes, g.scales, g.zeros, g.g_idx)
+    eg, er = O.recon_error(W, Qg, S64), O.recon_error(W, rep.Q, S64)
+    assert abs(eg - er) / er <= P.RECON_RTOL
+    ef = O.recon_error(W, free.Q, S64)
+    assert abs(eg - ef) / ef <= 0.02  # free-running: same quality
+    assert eg < O.recon_error(W, O.rtn(W, cfg).Q, S64)
+
+
+def test_identity_hessian_gives_rtn():
+    """P1 on the GPU: X with orthogonal rows of equal norm makes H a multiple
+    of I, so the GPU must reproduce round-to-nearest exactly."""
+    import torch
+    from post_weight_quantization_31_b300 import api
+    d_col, d_row = 256, 64
+    X = np.zeros((d_col, 512), dtype=np.float16)
+    X[np.arange(d_col), np.arange(d_col)] = 1.0
+    W = wl.make_weight(d_row, d_col, seed=3, dtype="bf16")
+    for kw in (dict(), dict(sym=True, bits=3, group_size=32), dict(group_size=-1, bits=2)):
+        cfg = qc(**kw)
+        g = P.gpu_solve(W, "bf16", X, cfg)
+        r = O.rtn(W, cfg)
+        assert np.array_equal(g.codes, r.codes), kw
+        assert np.array_equal(g.scales, r.scales), kw
+        assert np.array_equal(g.zeros, r.zeros), kw
+
+
+# ------------------------------------------------------------------ a5 alone
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+@pytest.mark.parametrize("d_row,d_col,gs", [(64, 256, 64), (96, 544, 32), (32, 4096, -1)])
+def test_pack_unpack_bit_exact(bits, d_row, d_col, gs):
+    import torch
+    from post_weight_quantization_31_b300 import api
+    rng = np.random.Generator(np.random.PCG64(bits * 1000 + d_col))
+    codes = rng.integers(0, 1 << bits, size=(d_row, d_col)).astype(np.uint8)
+    G = 1 if gs == -1 else d_col // gs
+    zeros = rng.integers(0, 1 << bits, size=(G, d_row)).astype(np.uint8)
+    qw, qz = api.pack(torch.from_numpy(codes).cuda(), torch.from_numpy(zeros).cuda(), bits, gs)
+    assert np.array_equal(qw.cpu().numpy(), O.pack_qweight(codes.astype(np.int64), bits))
+    assert np.array_equal(qz.cpu().numpy(), O.pack_qzeros(zeros.astype(np.int64), bits))
+    c2, z2 = api.unpack(qw, qz, d_row, d_col, bits, gs)
+    assert np.array_equal(c2.cpu().numpy(), codes)
+    assert np.array_equal(z2.cpu().numpy(), zeros)
