@@ -67,6 +67,13 @@ def hessian_accumulate(X: torch.Tensor, S: torch.Tensor, diag: torch.Tensor | No
     if X.dim() != 2 or X.stride(1) != 1:
         raise ValueError("X must be 2-D with tokens contiguous")
     d_col, n_tok = X.shape
+    if X.stride(0) % 8 != 0 or X.data_ptr() % 16 != 0:
+        # The library reads X with TMA, which needs 16-byte aligned rows:
+        # copy into storage whose row stride is a multiple of 8 halves.
+        ld = (n_tok + 7) // 8 * 8
+        Xp = torch.empty((d_col, ld), dtype=X.dtype, device=X.device)
+        Xp[:, :n_tok].copy_(X)
+        X = Xp[:, :n_tok]
     _need(S, torch.float32, "S", (d_col, d_col))
     _contig(S, "S")
     if diag is not None:
