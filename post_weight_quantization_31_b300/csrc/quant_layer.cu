@@ -24,7 +24,9 @@
 //              broadcast with one shuffle per column; group min/max by
 //              shuffles; writes codes (original column order), scales,
 //              zeros, and Err = the scaled errors of the block
-//     trailing W[:, i2:] -= Err U[i1:i2, i2:]  (fp32 FFMA tile GEMM)
+//     trailing W[:, i2:] -= Err U[i1:i2, i2:] on the tensor cores (3xTF32,
+//              fp32-accurate): A = Err (hi/lo, written by the column kernel),
+//              B = U^T rows (hi/lo, split once per call)
 //
 // Code decisions are taken in fp32 exactly as:
 //   s = (xmax - xmin) / maxq,  r = 1 / s,  z = rint(-xmin * r)   (asym)
@@ -36,7 +38,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
-#include "sgemm.cuh"
+#include "tgemm.cuh"
 
 namespace gptq {
 namespace {
@@ -149,7 +151,8 @@ struct ColumnArgs {
   uint8_t* codes;       // [d_row, d_col] original order
   float* scales;        // [G, d_row]
   uint8_t* zeros;       // [G, d_row]
-  float* Err;           // [d_row, CB]
+  float* Err_hi;        // [d_row, CB] scaled errors of the block, TF32 split
+  float* Err_lo;
 };
 
 __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) {
@@ -166,15 +169,21 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
   const int r = blockIdx.x * CL_ROWS + row_local;
   const int i1 = a.i1, nc = a.ncols, d = a.d_col;
 
-  // U block, rows/cols [i1, i1 + nc), padded by segment.
-  for (int idx = tid; idx < CB * CB; idx += CL_THREADS) {
-    const int jj = idx / CB, c = idx % CB;
-    float v = 0.f;
-    if (jj < nc && c < nc) v = a.U[static_cast<size_t>(i1 + jj) * d + i1 + c];
-    Us[jj * 4 * SEG + (c >> 5) * SEG + (c & 31)] = v;
+  // U block, rows/cols [i1, i1 + nc), padded by segment: 16-byte async
+  // copies (zero-filled outside the block), all in flight at once.
+  for (int q = tid; q < CB * (CB / 4); q += CL_THREADS) {
+    const int jj = q / (CB / 4), c4 = (q % (CB / 4)) * 4;
+    const bool inb = jj < nc && c4 < nc;
+    const float* src = inb ? a.U + static_cast<size_t>(i1 + jj) * d + i1 + c4 : a.U;
+    float* dst = Us + jj * 4 * SEG + (c4 >> 5) * SEG + (c4 & 31);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(inb ? 16 : 0)
+                 : "memory");
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   for (int jj = tid; jj < CB; jj += CL_THREADS)
-    inv_d[jj] = jj < nc ? 1.f / a.U[static_cast<size_t>(i1 + jj) * d + i1 + jj] : 0.f;
+    inv_d[jj] = jj < nc ? 1.f / Us[jj * 4 * SEG + (jj >> 5) * SEG + (jj & 31)] : 0.f;
 
   float w[32];
   const bool row_ok = r < a.d_row;
@@ -250,14 +259,33 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
     const int rl = idx / nc, c = idx % nc;
     const int rr = blockIdx.x * CL_ROWS + rl;
     if (rr >= a.d_row) continue;
-    a.Err[static_cast<size_t>(rr) * CB + c] = err_s[rl * (CB + 1) + c];
+    float h, l;
+    split_tf32(err_s[rl * (CB + 1) + c], h, l);
+    a.Err_hi[static_cast<size_t>(rr) * CB + c] = h;
+    a.Err_lo[static_cast<size_t>(rr) * CB + c] = l;
     a.codes[static_cast<size_t>(rr) * d + a.perm[i1 + c]] = code_s[rl * CB + c];
   }
 }
 
-__global__ void __launch_bounds__(GEMM_THREADS) trailing_kernel(GemmArgs g) {
-  __shared__ GemmSmem s;
-  gemm_tile<false, false, false>(g, blockIdx.y * GM, blockIdx.x * GN, s);
+// Ut = U^T split into TF32 hi/lo (32 x 32 tiles through shared memory).
+__global__ void transpose_split_kernel(const float* __restrict__ U, int d, float* __restrict__ Ut_hi,
+                                       float* __restrict__ Ut_lo) {
+  __shared__ float t[32][33];
+  const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int i = by + r, j = bx + threadIdx.x;
+    t[r][threadIdx.x] = (i < d && j < d) ? U[static_cast<size_t>(i) * d + j] : 0.f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int j = bx + r, i = by + threadIdx.x;
+    if (i < d && j < d) {
+      float h, l;
+      split_tf32(t[threadIdx.x][r], h, l);
+      Ut_hi[static_cast<size_t>(j) * d + i] = h;
+      Ut_lo[static_cast<size_t>(j) * d + i] = l;
+    }
+  }
 }
 
 }  // namespace
@@ -266,7 +294,7 @@ constexpr size_t kColumnSmem =
     sizeof(float) * (CB * 4 * SEG + CB + CL_ROWS * (CB + 1)) + CL_ROWS * CB;
 
 struct QuantLayout {
-  size_t status, Wf, Err, total;
+  size_t status, Wf, Err_hi, Err_lo, Ut_hi, Ut_lo, total;
 };
 
 static size_t align256q(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -278,8 +306,14 @@ static QuantLayout quant_layout(int64_t d_row, int64_t d_col) {
   off += 256;
   L.Wf = off;
   off = align256q(off + sizeof(float) * d_row * d_col);
-  L.Err = off;
+  L.Err_hi = off;
   off = align256q(off + sizeof(float) * d_row * CB);
+  L.Err_lo = off;
+  off = align256q(off + sizeof(float) * d_row * CB);
+  L.Ut_hi = off;
+  off = align256q(off + sizeof(float) * d_col * d_col);
+  L.Ut_lo = off;
+  off = align256q(off + sizeof(float) * d_col * d_col);
   L.total = off;
   return L;
 }
@@ -295,7 +329,10 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
   char* base = static_cast<char*>(ws);
   int* status = reinterpret_cast<int*>(base + L.status);
   float* Wf = reinterpret_cast<float*>(base + L.Wf);
-  float* Err = reinterpret_cast<float*>(base + L.Err);
+  float* Err_hi = reinterpret_cast<float*>(base + L.Err_hi);
+  float* Err_lo = reinterpret_cast<float*>(base + L.Err_lo);
+  float* Ut_hi = reinterpret_cast<float*>(base + L.Ut_hi);
+  float* Ut_lo = reinterpret_cast<float*>(base + L.Ut_lo);
   const float maxq = static_cast<float>((1 << cfg.bits) - 1);
   const int gs = cfg.group_size;
 
@@ -317,6 +354,11 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
     row_params_kernel<<<d_row, 256, 0, st>>>(Wf, d_col, maxq, cfg.sym, scales, zeros);
     GPTQ_LAUNCH_CHECK();
   }
+  {
+    dim3 grid((d_col + 31) / 32, (d_col + 31) / 32), block(32, 8);
+    transpose_split_kernel<<<grid, block, 0, st>>>(U, d_col, Ut_hi, Ut_lo);
+    GPTQ_LAUNCH_CHECK();
+  }
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(column_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kColumnSmem)));
   for (int i1 = 0; i1 < d_col; i1 += CB) {
@@ -335,25 +377,27 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
     ca.codes = codes;
     ca.scales = scales;
     ca.zeros = zeros;
-    ca.Err = Err;
+    ca.Err_hi = Err_hi;
+    ca.Err_lo = Err_lo;
     column_block_kernel<<<(d_row + CL_ROWS - 1) / CL_ROWS, CL_THREADS, kColumnSmem, st>>>(ca);
     GPTQ_LAUNCH_CHECK();
     const int i2 = i1 + nc;
     if (i2 < d_col) {
-      GemmArgs g;
+      TGemmArgs g;
       g.M = d_row;
       g.N = d_col - i2;
       g.K = nc;
       g.alpha = -1.f;
       g.beta = 1.f;
-      g.A = Err;
-      g.lda = CB;
-      g.B = U + static_cast<int64_t>(i1) * d_col + i2;
-      g.ldb = d_col;
       g.C = Wf + i2;
       g.ldc = d_col;
-      trailing_kernel<<<dim3((g.N + GN - 1) / GN, (g.M + GM - 1) / GM), GEMM_THREADS, 0, st>>>(g);
-      GPTQ_LAUNCH_CHECK();
+      g.lower = 0;
+      g.row_off = 0;
+      g.col_off = 0;
+      const gptq_status_t s = launch_tgemm_3xtf32(
+          Err_hi, Err_lo, CB, Ut_hi + static_cast<int64_t>(i2) * d_col + i1,
+          Ut_lo + static_cast<int64_t>(i2) * d_col + i1, d_col, g, st);
+      if (s != GPTQ_OK) return s;
     }
   }
   GPTQ_CUDA_TRY(cudaMemcpyAsync(status_host, status, sizeof(int), cudaMemcpyDeviceToHost, st));

@@ -1,0 +1,321 @@
+// 3xTF32 GEMM on tcgen05 (see tgemm.cuh for the contract).
+//
+// Structure (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: per 32-wide K slab, four 128 x 32 fp32 tiles
+//               (A_hi, A_lo, B_hi, B_lo) into a 3-stage ring, 128-byte swizzle
+//   warp 1      MMA issuer: per K slab, 4 steps of K=8, each three
+//               tcgen05.mma kind::tf32 (lo*hi, hi*lo, hi*hi) into TMEM
+//   warps 2-5   epilogue: TMEM -> registers -> C = alpha*acc + beta*C
+// Two 128-column TMEM accumulators let the epilogue of one tile overlap the
+// MMAs of the next.
+#include <algorithm>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "tgemm.cuh"
+
+namespace gptq {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 32;  // fp32: 128 bytes per row = one swizzle span
+constexpr int UK = 8;   // K of one kind::tf32 MMA
+constexpr int STAGES = 3;
+constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (BN == BM)
+constexpr int STAGE_BYTES = 4 * TILE_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t TMEM_COLS = 256;
+
+struct TGemmSched {
+  int m_tiles, n_tiles, k_blocks, tiles;
+};
+
+__device__ __forceinline__ int n_tiles_for_row(const TGemmArgs& a, const TGemmSched& s, int mt) {
+  if (!a.lower) return s.n_tiles;
+  const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM - 1 -
+                        a.col_off;
+  if (lim < 0) return 0;
+  return static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
+}
+
+__device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
+                                            int& nt) {
+  for (mt = 0; mt < s.m_tiles; ++mt) {
+    const int c = n_tiles_for_row(a, s, mt);
+    if (t < c) break;
+    t -= c;
+  }
+  nt = t;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tgemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
+                 const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
+                 TGemmArgs a, TGemmSched s, int* fault) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int i) { return bar0 + 8u * i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (STAGES + i); };
+  auto accf_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + i); };
+  auto acce_bar = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf_bar(i), 1);
+      mbar_init(acce_bar(i), 128);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_ahi);
+    tma_prefetch_desc(&tm_alo);
+    tma_prefetch_desc(&tm_bhi);
+    tma_prefetch_desc(&tm_blo);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < s.tiles; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(a, s, t, mt, nt);
+        for (int kb = 0; kb < s.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(sa + 0 * TILE_BYTES, &tm_ahi, fb, kb * BK, mt * BM);
+          tma_load_2d(sa + 1 * TILE_BYTES, &tm_alo, fb, kb * BK, mt * BM);
+          tma_load_2d(sa + 2 * TILE_BYTES, &tm_bhi, fb, kb * BK, nt * BN);
+          tma_load_2d(sa + 3 * TILE_BYTES, &tm_blo, fb, kb * BK, nt * BN);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(BM, BN, /*tf32*/ 2, /*tf32*/ 2);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < s.tiles; t += gridDim.x) {
+        if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, fault)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < s.k_blocks; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, fault)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t d_ahi = smem_desc_sw128_kmajor(sa + 0 * TILE_BYTES);
+          const uint64_t d_alo = smem_desc_sw128_kmajor(sa + 1 * TILE_BYTES);
+          const uint64_t d_bhi = smem_desc_sw128_kmajor(sa + 2 * TILE_BYTES);
+          const uint64_t d_blo = smem_desc_sw128_kmajor(sa + 3 * TILE_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t off = static_cast<uint64_t>((k * UK * 4) >> 4);  // 32 bytes per step
+            const uint32_t first = (kb == 0 && k == 0) ? 0u : 1u;
+            tc_mma_tf32(d_tmem, d_alo + off, d_bhi + off, idesc, first);
+            tc_mma_tf32(d_tmem, d_ahi + off, d_blo + off, idesc, 1u);
+            tc_mma_tf32(d_tmem, d_ahi + off, d_bhi + off, idesc, 1u);
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      tc_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, fault);
+    }
+  } else {
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < s.tiles; t += gridDim.x) {
+      int mt, nt;
+      tile_coords(a, s, t, mt, nt);
+      if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) break;
+      tc_fence_after();
+      const int m = mt * BM + q * 32 + lane;
+      const bool row_ok = m < a.M;
+      const long long diag = static_cast<long long>(a.row_off) + m - a.col_off;  // n <= diag
+      float* crow = a.C + static_cast<int64_t>(m) * a.ldc;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n0 = nt * BN + c * 32;
+        if (n0 >= a.N) break;
+        float v[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(acc * BN + c * 32),
+                           v);
+        if (!row_ok) continue;
+        const bool full = (n0 + 32 <= a.N) && (!a.lower || n0 + 31 <= diag);
+        if (full && (a.ldc % 4 == 0)) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4* p = reinterpret_cast<float4*>(crow + n0 + i);
+            float4 o = make_float4(a.alpha * v[i], a.alpha * v[i + 1], a.alpha * v[i + 2],
+                                   a.alpha * v[i + 3]);
+            if (a.beta != 0.f) {
+              const float4 cv = *p;
+              o.x = fmaf(a.beta, cv.x, o.x);
+              o.y = fmaf(a.beta, cv.y, o.y);
+              o.z = fmaf(a.beta, cv.z, o.z);
+              o.w = fmaf(a.beta, cv.w, o.w);
+            }
+            *p = o;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int n = n0 + i;
+            if (n >= a.N || (a.lower && n > diag)) continue;
+            float o = a.alpha * v[i];
+            if (a.beta != 0.f) o = fmaf(a.beta, crow[n], o);
+            crow[n] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acce_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool make_f32_map(CUtensorMap* m, const float* base, int64_t rows, int64_t k, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
+  cuuint32_t box[2] = {BK, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TGemmSched make_sched(const TGemmArgs& a) {
+  TGemmSched s;
+  s.m_tiles = (a.M + BM - 1) / BM;
+  s.n_tiles = (a.N + BN - 1) / BN;
+  s.k_blocks = (a.K + BK - 1) / BK;
+  s.tiles = 0;
+  for (int mt = 0; mt < s.m_tiles; ++mt) {
+    int c = s.n_tiles;
+    if (a.lower) {
+      const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM -
+                            1 - a.col_off;
+      c = lim < 0 ? 0 : static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
+    }
+    s.tiles += c;
+  }
+  return s;
+}
+
+}  // namespace
+
+int tgemm_tile_count(const TGemmArgs& args) { return make_sched(args).tiles; }
+
+gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
+                                  const float* B_lo, int64_t ldb, const TGemmArgs& args,
+                                  cudaStream_t st) {
+  if (args.M <= 0 || args.N <= 0 || args.K <= 0) return GPTQ_OK;
+  const TGemmSched s = make_sched(args);
+  if (s.tiles == 0) return GPTQ_OK;
+  CUtensorMap m_ahi, m_alo, m_bhi, m_blo;
+  if (!make_f32_map(&m_ahi, A_hi, args.M, args.K, lda) || !make_f32_map(&m_alo, A_lo, args.M, args.K, lda) ||
+      !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb) || !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb))
+    return GPTQ_ERR_CUDA;
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     SMEM_BYTES));
+  const int grid = std::min(sm_count(), s.tiles);
+  tgemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m_ahi, m_alo, m_bhi, m_blo, args, s,
+                                                      fault_word_ptr());
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}
+
+}  // namespace gptq
+
+// Test hook (not part of the public header): C = alpha A B^T + beta C with
+// A, B given as TF32 hi/lo pairs, on `stream`.
+extern "C" GPTQ_API int gptq_internal_tgemm(const float* A_hi, const float* A_lo, int64_t lda,
+                                            const float* B_hi, const float* B_lo, int64_t ldb, int M,
+                                            int N, int K, float alpha, float beta, float* C,
+                                            int64_t ldc, int lower, int row_off, int col_off,
+                                            gptq_stream_t stream) {
+  gptq::TGemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.alpha = alpha;
+  g.beta = beta;
+  g.C = C;
+  g.ldc = ldc;
+  g.lower = lower;
+  g.row_off = row_off;
+  g.col_off = col_off;
+  return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}

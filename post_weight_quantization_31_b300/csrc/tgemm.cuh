@@ -1,0 +1,47 @@
+// fp32-accurate GEMM on the 5th-generation tensor cores ("3xTF32").
+//
+//   C[m, n] = alpha * sum_k A[m, k] B[n, k] + beta * C[m, n]
+//
+// A [M, K] and B [N, K] are row-major (K contiguous, "K-major") and each is
+// given as two fp32 arrays hi + lo with hi exactly representable in TF32
+// (10-bit mantissa) and lo = x - hi; see split_tf32().  The product is
+// formed as A_lo B_hi + A_hi B_lo + A_hi B_hi with fp32 accumulation in
+// TMEM, which keeps about 2^-21 relative accuracy per product (the dropped
+// A_lo B_lo term is ~2^-22).  With `lower`, only elements with
+// row_off + m >= col_off + n are written, and tiles entirely above that
+// diagonal are skipped.
+//
+// Requirements: K % 32 == 0 is not needed (TMA zero-fills), but lda, ldb
+// (elements) must be multiples of 4 and A/B 16-byte aligned; ldc any.
+#pragma once
+
+#include "common.cuh"
+
+namespace gptq {
+
+struct TGemmArgs {
+  int M, N, K;
+  float alpha, beta;
+  float* C;
+  int64_t ldc;
+  int lower;
+  int row_off, col_off;
+};
+
+// hi: x rounded to a TF32 value (10 explicit mantissa bits, ties away);
+// lo: x - hi, exact in fp32.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  const uint32_t u = __float_as_uint(x);
+  hi = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
+  if (!isfinite(hi)) hi = __uint_as_float(u & 0xFFFFE000u);
+  lo = __fsub_rn(x, hi);
+}
+
+gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda,
+                                  const float* B_hi, const float* B_lo, int64_t ldb,
+                                  const TGemmArgs& args, cudaStream_t st);
+
+// Number of 128 x 128 output tiles the launch above would process.
+int tgemm_tile_count(const TGemmArgs& args);
+
+}  // namespace gptq
