@@ -41,6 +41,13 @@ WORKLOAD = ("7B attention projection: W bf16 4096x4096 N(0,0.02^2); X fp16 4096x
             "desc_act off")
 
 
+def set_tokens(n: int) -> None:
+    """Shrinks the calibration set (profiling cases only)."""
+    global N_TOK, WORKLOAD
+    WORKLOAD = WORKLOAD.replace(f"4096x{N_TOK}", f"4096x{n}") + " (profiling case)"
+    N_TOK = n
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -56,7 +63,7 @@ def measured_peaks() -> dict:
 class ClockSampler:
     """nvidia-smi samples during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -68,7 +75,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -84,17 +91,27 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
+    def mark(self, which: str) -> None:
+        """Wall-clock bounds of the timed region (samples outside are dropped)."""
+        setattr(self, which, time.time())
+
     def summary(self) -> dict:
+        import datetime
         rows = []
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), active=parts[4],
-                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append(dict(ts=ts, sm=float(parts[2]), smax=float(parts[3]), active=parts[5],
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
             except ValueError:
                 continue
+        t0, t1 = getattr(self, "start", None), getattr(self, "end", None)
+        if rows and t0 is not None and t1 is not None:
+            inside = [r for r in rows if t0 - 0.05 <= r["ts"] <= t1 + 0.05]
+            rows = inside or sorted(rows, key=lambda r: abs(r["ts"] - 0.5 * (t0 + t1)))[:1]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         reasons = set()
@@ -151,23 +168,26 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         if ev is not None:
             ev[4].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    n0 = api.launch_count()
+    # The sampler starts before the warm-up so that it is running when the
+    # timed region begins; only samples inside that region are kept.
     with ClockSampler(local_rank) as clk:
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        n0 = api.launch_count()
+        clk.mark("start")
         t_start.record(stream)
         for k in range(args.steps):
             step(evs[k])
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark("end")
     if dist is not None:
         dist.barrier()
     launches = api.launch_count() - n0
@@ -323,7 +343,12 @@ def main() -> None:
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     ap.add_argument("--syrk-traffic", type=float, default=None,
                     help="DRAM bytes per Hessian launch from an ncu capture")
+    ap.add_argument("--tokens", type=int, default=N_TOK,
+                    help="calibration tokens (smaller values make a profiling case, "
+                         "not the benchmark workload)")
     args = ap.parse_args()
+    if args.tokens != N_TOK:
+        set_tokens(args.tokens)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
