@@ -157,6 +157,31 @@ GPTQ_API gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int
                                 const gptq_config_t* cfg, float* U, int32_t* perm,
                                 void* ws, size_t ws_bytes, gptq_stream_t stream);
 
+/*
+ * gptq_prepare_hinv without a caller workspace.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory when they need the factor -- code that runs inside another
+ * framework's memory pool and may not allocate outside it, or a
+ * latency-critical path where cudaMalloc / cudaFree would synchronize the
+ * device.  It computes exactly what gptq_prepare_hinv computes, with the
+ * same arguments except ws / ws_bytes, and allocates nothing: the scratch
+ * space is a fixed array of about 5.3 MB that the library keeps in device
+ * memory on every GPU it is loaded on, until the process exits.
+ *   d_col   at most GPTQ_NOALLOC_MAX_D_COL (1024); larger values return
+ *           GPTQ_ERR_WORKSPACE with no side effect.  Other argument errors
+ *           and status codes are those of gptq_prepare_hinv.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Every call, from any thread or stream,
+ *   shares the one array and leaves its contents behind: calls whose GPU
+ *   work overlaps (two streams, two host threads) race and corrupt each
+ *   other's results, so serialize them.  Synchronizes `stream`.
+ */
+#define GPTQ_NOALLOC_MAX_D_COL 1024
+GPTQ_API gptq_status_t gptq_prepare_hinv_noalloc(const float* S, const double* diag, int64_t d_col,
+                                                 int64_t n_seen, const gptq_config_t* cfg, float* U,
+                                                 int32_t* perm, gptq_stream_t stream);
+
 /* Bytes of workspace gptq_quantize_layer needs. */
 GPTQ_API size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const gptq_config_t* cfg);
 

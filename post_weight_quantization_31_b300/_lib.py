@@ -23,6 +23,7 @@ STATUS_NAMES = {
     7: "GPTQ_ERR_UNSUPPORTED",
 }
 W_FP32, W_BF16, W_FP16 = 0, 1, 2
+NOALLOC_MAX_D_COL = 1024  # GPTQ_NOALLOC_MAX_D_COL in include/gptq.h
 
 # Every function the header declares, with (restype, argtypes).
 _vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
@@ -41,6 +42,7 @@ SIGNATURES = {
                                        ctypes.POINTER(ctypes.c_int64), _vp]),
     "gptq_prepare_workspace_size": (_sz, [_i64]),
     "gptq_prepare_hinv": (_i32, [_vp, _vp, _i64, _i64, _CFGP, _vp, _vp, _vp, _sz, _vp]),
+    "gptq_prepare_hinv_noalloc": (_i32, [_vp, _vp, _i64, _i64, _CFGP, _vp, _vp, _vp]),
     "gptq_quantize_workspace_size": (_sz, [_i64, _i64, _CFGP]),
     "gptq_quantize_layer": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _CFGP, _vp, _vp, _vp, _vp,
                                    _vp, _sz, _vp]),

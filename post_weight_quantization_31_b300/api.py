@@ -109,6 +109,23 @@ def prepare_hinv(S: torch.Tensor, n_seen: int, cfg: QuantConfig, diag: torch.Ten
     return U, perm
 
 
+def prepare_hinv_noalloc(S: torch.Tensor, n_seen: int, cfg: QuantConfig, U: torch.Tensor,
+                         perm: torch.Tensor, diag: torch.Tensor | None = None):
+    """prepare_hinv for callers that cannot allocate device memory: U and perm
+    are the caller's, the scratch space is the library's own fixed array
+    (d_col <= 1024).  Calls whose GPU work overlaps share that array and race."""
+    lib = _lib.load()
+    d = S.shape[0]
+    _need(S, torch.float32, "S", (d, d))
+    _need(U, torch.float32, "U", (d, d))
+    _need(perm, torch.int32, "perm", (d,))
+    c = _lib.make_config(cfg)
+    _check(lib.gptq_prepare_hinv_noalloc(S.data_ptr(), _ptr(diag), d, int(n_seen), ctypes.byref(c),
+                                         U.data_ptr(), perm.data_ptr(), _stream()),
+           "gptq_prepare_hinv_noalloc")
+    return U, perm
+
+
 # ----------------------------------------------------------------------- a3/a4
 def quantize_workspace_size(d_row: int, d_col: int, cfg: QuantConfig) -> int:
     c = _lib.make_config(cfg)
