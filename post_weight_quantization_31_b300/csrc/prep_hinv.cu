@@ -170,116 +170,233 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                : "memory");
 }
 
-// Factor the b x b lower block D = Z[k..k+b)^2 and write Mt = (L^-1)^T
-// (upper triangular, zeros below) to shared memory.
+// Factor the b x b lower block D = Z[k..k+b)^2 (b a multiple of 32, at most
+// NB) and write Mt = (L^-1)^T (Mt[c][i] = L^-1[i][c], zero above the
+// diagonal of L^-1 and outside b) to shared memory.
 //
-// One right-looking pass over the columns j, on a matrix G held in
-// registers (4 x 8 per thread) whose columns < j hold the running
-// right-hand side x of L x = I and whose columns >= j hold the Schur
-// complement a.  Step j is the rank-1 update of the rows i > j
-//   G[i][c] -= (a_ij / a_jj) V[c],   V[c] = x_jc (c < j), a_cj (c > j),
-// with G[i][j] set to -a_ij / a_jj (x_ij = 0 - l_ij x_jj, x_jj = 1).  The
-// owners of row j and column j publish V (double-buffered) and the pivot
-// a_jj; one barrier per column.  At the end L^-1[i][c] = x_ic / sqrt(a_ii).
-__device__ bool factor_invert_regs(const float* __restrict__ Z, int64_t ldz, int k, int b,
-                                   float* __restrict__ Mt, float* __restrict__ V,
-                                   float* __restrict__ piv) {
-  const int t = threadIdx.x, rg = t >> 4, cg = t & 15;
-  const int r0 = 4 * rg, c0 = 8 * cg;
-  const int wmax = ((t >> 5) << 3) + 7;  // last row of this warp
-  float g[4][8];
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = r0 + ii;
-    float4 lo4 = make_float4(0.f, 0.f, 0.f, 0.f), hi4 = lo4;
-    if (i < b && c0 <= i) {
-      const float* src = Z + static_cast<int64_t>(k + i) * ldz + k + c0;
-      lo4 = *reinterpret_cast<const float4*>(src);
-      if (c0 + 4 <= i) hi4 = *reinterpret_cast<const float4*>(src + 4);
-    }
-    const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) g[ii][cc] = (c0 + cc <= i && i < b) ? v[cc] : 0.f;
+// Blocked over 32-wide sub-panels s, so that the column-by-column chain of
+// the factorization runs inside one warp and block barriers are needed only
+// between the sub-panel phases:
+//   F  one warp factors the 32 x 32 diagonal sub-block in registers (lane i
+//      holds row i; each column's entries are broadcast by shuffles);
+//   T  the rows below, one thread per row, solve x L_ss^T = d by forward
+//      substitution (L_ts = D_ts L_ss^-T);
+//   U  the trailing sub-blocks of the diagonal block get D_tu -= L_ts L_us^T.
+// Then L^-1 is built by blocks: the inverse of each diagonal sub-block by
+// one warp (back substitution per row, no cross-lane traffic), and the
+// sub-blocks below the diagonal level by level,
+//   M_ts = -M_tt sum_{u=s}^{t-1} L_tu M_us.
+// Returns true (in thread 0) if a pivot was not positive.
+constexpr int TMLD = 36;  // row stride of the 32 x 32 level products
+
+__device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, int k, int b,
+                                      float* __restrict__ Mt, float* __restrict__ Ls,
+                                      float* __restrict__ rinv, float* __restrict__ Tm,
+                                      float* __restrict__ LT, float* __restrict__ colbuf) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int nsub = b >> 5;
+  for (int q = t; q < NB * (NB / 4); q += PT) {
+    const int i = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < b && c4 <= i) v = *reinterpret_cast<const float4*>(Z + static_cast<int64_t>(k + i) * ldz + k + c4);
+    *reinterpret_cast<float4*>(Ls + i * LDM + c4) = v;
+    *reinterpret_cast<float4*>(Mt + i * LDM + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  // publish for column j: pivot, row j (c < j) and column j (i > j) into V[j & 1]
-  auto publish = [&](int j) {
-    float* vb = V + (j & 1) * NB;
-    if (rg == (j >> 2)) {
+  __syncthreads();
+  bool bad = false;
+  for (int s = 0; s < nsub; ++s) {
+    const int c0 = 32 * s;
+    if (warp == 0) {
+      // ---- F: Cholesky of the diagonal sub-block, lane = row
+      float a[32];
+      float* row = Ls + (c0 + lane) * LDM + c0;
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        if (r0 + ii != j) continue;
+      for (int c = 0; c < 32; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(row + c);
+        a[c] = v.x;
+        a[c + 1] = v.y;
+        a[c + 2] = v.z;
+        a[c + 3] = v.w;
+      }
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int c = c0 + cc;
-          if (c < j) vb[c] = g[ii][cc];
-          if (c == j) {
-            piv[j] = g[ii][cc];
-            g[ii][cc] = 1.f;  // x_jj
+      for (int c = 0; c < 32; ++c)
+        if (c > lane) a[c] = 0.f;
+      float my_r = 1.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float ajj = __shfl_sync(0xffffffffu, a[j], j);
+        if (!(ajj > 0.f)) {
+          bad = true;
+          ajj = 1.f;
+        }
+        const float r = rsqrtf(ajj);  // 1 / l_jj
+        if (lane == j) my_r = r;
+        const float l = (lane == j) ? ajj * r : a[j] * r;  // l_ij for lanes i >= j
+        a[j] = (lane >= j) ? l : 0.f;
+        // column j of L to every lane (double-buffered: one warp barrier per column)
+        float* cb = colbuf + (j & 1) * 32;
+        cb[lane] = l;
+        __syncwarp();
+#pragma unroll
+        for (int c4 = (j + 1) & ~3; c4 < 32; c4 += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(cb + c4);
+          const float lc[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (c4 + e > j) a[c4 + e] = fmaf(-l, lc[e], a[c4 + e]);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 4)
+        *reinterpret_cast<float4*>(row + c) =
+            make_float4(c <= lane ? a[c] : 0.f, c + 1 <= lane ? a[c + 1] : 0.f,
+                        c + 2 <= lane ? a[c + 2] : 0.f, c + 3 <= lane ? a[c + 3] : 0.f);
+      rinv[c0 + lane] = my_r;
+    }
+    __syncthreads();
+    // ---- T: rows below the sub-block, within the diagonal block
+    if (t < b - c0 - 32) {
+      float* row = Ls + (c0 + 32 + t) * LDM + c0;
+      float a[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(row + c);
+        a[c] = v.x;
+        a[c + 1] = v.y;
+        a[c + 2] = v.z;
+        a[c + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float x = a[c] * rinv[c0 + c];
+        a[c] = x;
+#pragma unroll
+        for (int m = c + 1; m < 32; ++m) a[m] = fmaf(-x, Ls[(c0 + m) * LDM + c0 + c], a[m]);
+      }
+#pragma unroll
+      for (int c = 0; c < 32; c += 4)
+        *reinterpret_cast<float4*>(row + c) = make_float4(a[c], a[c + 1], a[c + 2], a[c + 3]);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) LT[c * LDM + c0 + 32 + t] = a[c];
+    }
+    __syncthreads();
+    // ---- U: D_tu -= L_ts L_us^T for s < u <= t < nsub, 4 x 4 register tiles
+    //      with both operands read along rows of the transposed sub-panel LT
+    const int nt = nsub - s - 1;
+    const int npairs = nt * (nt + 1) / 2;
+    if (t < npairs * 64) {
+      int pi = t >> 6;
+      int tt = s + 1;
+      while (pi > tt - s - 1) {  // pairs ordered (s+1,s+1), (s+2,s+1), (s+2,s+2), ...
+        pi -= tt - s;
+        ++tt;
+      }
+      const int uu = s + 1 + pi;
+      const int i0 = 32 * tt + 4 * ((t >> 3) & 7), j0 = 32 * uu + 4 * (t & 7);
+      float acc[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+#pragma unroll 8
+      for (int m = 0; m < 32; ++m) {
+        const float4 x = *reinterpret_cast<const float4*>(LT + m * LDM + i0);
+        const float4 y = *reinterpret_cast<const float4*>(LT + m * LDM + j0);
+        const float xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(xv[r], yv[c], acc[r][c]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float4* o = reinterpret_cast<float4*>(Ls + (i0 + r) * LDM + j0);
+        float4 v = *o;
+        v.x -= acc[r][0];
+        v.y -= acc[r][1];
+        v.z -= acc[r][2];
+        v.w -= acc[r][3];
+        *o = v;
+      }
+    }
+    __syncthreads();
+  }
+  // ---- inverse of each diagonal sub-block: lane i computes row i of M_ww
+  if (warp < nsub) {
+    const int w0 = 32 * warp;
+    float acc[32], y[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) acc[c] = (c == lane) ? 1.f : 0.f;
+#pragma unroll
+    for (int m = 31; m >= 0; --m) {
+      const float ym = (m <= lane) ? acc[m] * rinv[w0 + m] : 0.f;
+      y[m] = ym;
+#pragma unroll
+      for (int c = 0; c < m; ++c) acc[c] = fmaf(-ym, Ls[(w0 + m) * LDM + w0 + c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) Mt[(w0 + c) * LDM + w0 + lane] = y[c];
+  }
+  __syncthreads();
+  // ---- sub-blocks below the diagonal of L^-1, one level t - s at a time
+  for (int lv = 1; lv < nsub; ++lv) {
+    const int npair = nsub - lv;
+    const int p = t >> 7, i = t & 31, cg8 = ((t >> 5) & 3) * 8;
+    const int sb = p, tb = p + lv;
+    if (p < npair) {
+      // Tm[p] = sum_{u=sb}^{tb-1} L_{tb,u} M_{u,sb}
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int u = sb; u < tb; ++u) {
+        const float* li = Ls + (32 * tb + i) * LDM + 32 * u;
+#pragma unroll 2
+        for (int m = 0; m < 32; m += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(li + m);
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            const float4 y = *reinterpret_cast<const float4*>(Mt + (32 * sb + cg8 + cc) * LDM + 32 * u + m);
+            acc[cc] = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc[cc]))));
           }
         }
       }
+      float* tm = Tm + (p * 32 + i) * TMLD + cg8;
+      *reinterpret_cast<float4*>(tm) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(tm + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
-    if (cg == (j >> 3)) {
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        if (c0 + cc != j) continue;
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-          if (r0 + ii > j) vb[r0 + ii] = g[ii][cc];
+    __syncthreads();
+    if (p < npair) {
+      // M_{tb,sb} = -M_{tb,tb} Tm[p]
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int m = 0; m < 32; ++m) {
+        const float mv = Mt[(32 * tb + m) * LDM + 32 * tb + i];
+        const float4 y0 = *reinterpret_cast<const float4*>(Tm + (p * 32 + m) * TMLD + cg8);
+        const float4 y1 = *reinterpret_cast<const float4*>(Tm + (p * 32 + m) * TMLD + cg8 + 4);
+        acc[0] = fmaf(mv, y0.x, acc[0]);
+        acc[1] = fmaf(mv, y0.y, acc[1]);
+        acc[2] = fmaf(mv, y0.z, acc[2]);
+        acc[3] = fmaf(mv, y0.w, acc[3]);
+        acc[4] = fmaf(mv, y1.x, acc[4]);
+        acc[5] = fmaf(mv, y1.y, acc[5]);
+        acc[6] = fmaf(mv, y1.z, acc[6]);
+        acc[7] = fmaf(mv, y1.w, acc[7]);
       }
-    }
-  };
-  publish(0);
-  __syncthreads();
-  bool notpd = false;
-  for (int j = 0; j < b; ++j) {
-    const float* vb = V + (j & 1) * NB;
-    float ajj = piv[j];
-    if (!(ajj > 0.f)) {
-      notpd = true;
-      ajj = 1.f;
-    }
-    if (wmax > j) {
-      const float inv = 1.f / ajj;
-      const float4 va = *reinterpret_cast<const float4*>(vb + c0);
-      const float4 vb4 = *reinterpret_cast<const float4*>(vb + c0 + 4);
-      const float4 vr = *reinterpret_cast<const float4*>(vb + r0);
-      const float vc[8] = {va.x, va.y, va.z, va.w, vb4.x, vb4.y, vb4.z, vb4.w};
-      const float rv[4] = {vr.x, vr.y, vr.z, vr.w};
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        if (r0 + ii <= j) continue;
-        const float l = rv[ii] * inv;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          g[ii][cc] = (c0 + cc == j) ? -l : fmaf(-l, vc[cc], g[ii][cc]);
-      }
+      for (int cc = 0; cc < 8; ++cc) Mt[(32 * sb + cg8 + cc) * LDM + 32 * tb + i] = -acc[cc];
     }
-    if (j + 1 < b) publish(j + 1);
     __syncthreads();
   }
-  // Mt[c][i] = L^-1[i][c] = x_ic / sqrt(a_ii) for c <= i < b, else 0.
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = r0 + ii;
-    const float p = (i < b) ? piv[i] : 1.f;
-    const float sc = 1.f / sqrtf(p > 0.f ? p : 1.f);
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      const int c = c0 + cc;
-      Mt[c * LDM + i] = (c <= i && i < b) ? g[ii][cc] * sc : 0.f;
-    }
-  }
-  __syncthreads();
-  return notpd;
+  return bad;
 }
 
 __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   extern __shared__ __align__(16) float sm[];
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
-  float* V = T + NB * LDM;           // [2][NB]
-  float* piv = V + 2 * NB;           // [NB]
+  float* Ls = T + NB * LDM;          // [NB][LDM]  diagonal block, then L_kk
+  float* rinv = Ls + NB * LDM;       // [NB]       1 / diag(L_kk)
+  float* Tm = rinv + NB;             // [3][32][TMLD] level products
+  float* LT = Tm;                    // [32][LDM] transposed sub-panel (shares Tm's space)
+  float* colbuf = LT + 32 * LDM;     // [2][32]
   const int n = p.n, k = p.k, b = p.b;
   const int64_t ldz = n;
   const int t = threadIdx.x, rg = t >> 4, cg = t & 15;
@@ -306,7 +423,7 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
-  const bool notpd = factor_invert_regs(p.Z, ldz, k, b, Mt, V, piv);
+  const bool notpd = factor_invert_blocked(p.Z, ldz, k, b, Mt, Ls, rinv, Tm, LT, colbuf);
   if (role == 0 && t == 0 && notpd) atomicOr(p.status, kStatNotPD);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
@@ -456,7 +573,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
                                                 status);
     GPTQ_LAUNCH_CHECK();
   }
-  const size_t smem = sizeof(float) * (2 * NB * LDM + 3 * NB);
+  const size_t smem = sizeof(float) * (3 * NB * LDM + NB + 32 * LDM + 64);
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
   for (int k = 0; k < d; k += NB) {
