@@ -19,14 +19,18 @@
 //              initial row
 //   per 128-column block [i1, i2):
 //     column   row-parallel sequential loop over the block's columns:
-//              4 lanes own one row (32 columns each, in registers), the
+//              16 lanes own one row (8 columns each, in registers), the
 //              block of U sits in shared memory, the pivot column's value is
 //              broadcast with one shuffle per column; group min/max by
 //              shuffles; writes codes (original column order), scales,
 //              zeros, and Err = the scaled errors of the block
 //     trailing W[:, i2:] -= Err U[i1:i2, i2:] on the tensor cores (3xTF32,
-//              fp32-accurate): A = Err (hi/lo, written by the column kernel),
-//              B = U^T rows (hi/lo, split once per call)
+//              fp32-accurate), in two levels: inside each 512-column
+//              super-block after every block, and for all columns right of
+//              the super-block once per super-block with K = 512 (the same
+//              sum in another order; a quarter of the read-modify-write
+//              traffic on W).  A = Err (hi/lo, written by the column
+//              kernel), B = U^T rows (hi/lo, split once per call)
 //
 // Code decisions are taken in fp32 exactly as:
 //   s = (xmax - xmin) / maxq,  r = 1 / s,  z = rint(-xmin * r)   (asym)
@@ -43,12 +47,14 @@
 namespace gptq {
 namespace {
 
-constexpr int CB = 128;           // block width (blocksize)
-constexpr int SEG = 36;           // padded 32-column segment of a U row in smem
-constexpr int ROWS_PER_WARP = 8;  // 4 lanes per row
-constexpr int CL_WARPS = 2;
-constexpr int CL_ROWS = CL_WARPS * ROWS_PER_WARP;
-constexpr int CL_THREADS = CL_WARPS * 32;
+constexpr int CB = 128;            // block width (blocksize)
+constexpr int SB = 4 * CB;         // super-block of the two-level lazy update
+constexpr int LPR = 16;            // lanes per row
+constexpr int CPL = CB / LPR;      // columns of a row held by one lane (registers)
+constexpr int USEG = CPL + 4;      // padded 8-column segment of a U row in smem
+constexpr int UROW = LPR * USEG;   // padded U row
+constexpr int CL_THREADS = 256;
+constexpr int CL_ROWS = CL_THREADS / LPR;
 
 struct QParams {
   float s, r, z;
@@ -151,21 +157,22 @@ struct ColumnArgs {
   uint8_t* codes;       // [d_row, d_col] original order
   float* scales;        // [G, d_row]
   uint8_t* zeros;       // [G, d_row]
-  float* Err_hi;        // [d_row, CB] scaled errors of the block, TF32 split
-  float* Err_lo;
+  float* Err_hi;        // [d_row, SB] scaled errors of the super-block, TF32 split;
+  float* Err_lo;        // this block writes columns [err_col0, err_col0 + ncols)
+  int err_col0;
 };
 
 __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) {
-  extern __shared__ float smem[];
-  float* Us = smem;                                  // [CB][4 * SEG]
-  float* inv_d = Us + CB * 4 * SEG;                  // [CB]
+  extern __shared__ __align__(16) float smem[];
+  float* Us = smem;                                  // [CB][UROW]
+  float* inv_d = Us + CB * UROW;                     // [CB]
   float* err_s = inv_d + CB;                         // [CL_ROWS][CB + 1]
   uint8_t* code_s = reinterpret_cast<uint8_t*>(err_s + CL_ROWS * (CB + 1));  // [CL_ROWS][CB]
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int row_local = (tid >> 5) * ROWS_PER_WARP + (lane >> 2);
-  const int sub = lane & 3;
+  const int row_local = tid / LPR;
+  const int sub = lane % LPR;  // this lane holds columns [CPL*sub, CPL*sub + CPL) of the block
   const int r = blockIdx.x * CL_ROWS + row_local;
   const int i1 = a.i1, nc = a.ncols, d = a.d_col;
 
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
     const int jj = q / (CB / 4), c4 = (q % (CB / 4)) * 4;
     const bool inb = jj < nc && c4 < nc;
     const float* src = inb ? a.U + static_cast<size_t>(i1 + jj) * d + i1 + c4 : a.U;
-    float* dst = Us + jj * 4 * SEG + (c4 >> 5) * SEG + (c4 & 31);
+    float* dst = Us + jj * UROW + (c4 / CPL) * USEG + (c4 % CPL);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
                  "r"(inb ? 16 : 0)
                  : "memory");
@@ -183,15 +190,15 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   for (int jj = tid; jj < CB; jj += CL_THREADS)
-    inv_d[jj] = jj < nc ? 1.f / Us[jj * 4 * SEG + (jj >> 5) * SEG + (jj & 31)] : 0.f;
+    inv_d[jj] = jj < nc ? 1.f / Us[jj * UROW + (jj / CPL) * USEG + (jj % CPL)] : 0.f;
 
-  float w[32];
+  float w[CPL];
   const bool row_ok = r < a.d_row;
-  const float* wrow = a.Wf + static_cast<size_t>(r) * d + i1 + 32 * sub;
+  const float* wrow = a.Wf + static_cast<size_t>(r) * d + i1 + CPL * sub;
 #pragma unroll
-  for (int k = 0; k < 32; k += 4) {
+  for (int k = 0; k < CPL; k += 4) {
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row_ok && 32 * sub + k < nc) v = *reinterpret_cast<const float4*>(wrow + k);
+    if (row_ok && CPL * sub + k < nc) v = *reinterpret_cast<const float4*>(wrow + k);
     w[k] = v.x;
     w[k + 1] = v.y;
     w[k + 2] = v.z;
@@ -205,27 +212,31 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
   }
   __syncthreads();
 
-  const int src_base = lane & ~3;
-  for (int sub0 = 0; sub0 < (nc >> 5); ++sub0) {
-    const int seg_start = i1 + 32 * sub0;
+  float e_own[CPL], q_own[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) e_own[k] = q_own[k] = 0.f;
+  const int src_base = lane & ~(LPR - 1);
+  for (int seg = 0; seg < nc / CPL; ++seg) {
+    const int seg_start = i1 + CPL * seg;
     const bool gstart = a.gs > 0 && (seg_start % a.gs) == 0;
-    const float* urow_base = Us + (32 * sub0) * 4 * SEG + sub * SEG;
+    const float* urow_base = Us + (CPL * seg) * UROW + sub * USEG;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < CPL; ++k) {
       if (k == 0 && gstart) {
-        // Group [seg_start, seg_start + gs): lanes sub0 .. sub0 + gs/32 - 1.
+        // Group [seg_start, seg_start + gs): lanes seg .. seg + gs/CPL - 1 of the row.
         float mn = INFINITY, mx = -INFINITY;
-        if (sub >= sub0 && sub < sub0 + (a.gs >> 5)) {
+        if (sub >= seg && sub < seg + a.gs / CPL) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
+          for (int t = 0; t < CPL; ++t) {
             mn = fminf(mn, w[t]);
             mx = fmaxf(mx, w[t]);
           }
         }
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+#pragma unroll
+        for (int o = 1; o < LPR; o <<= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
         p = grid_params(mn, mx, a.maxq, a.sym);
         if (sub == 0 && row_ok) {
           const int g = seg_start / a.gs;
@@ -233,25 +244,33 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
           a.zeros[static_cast<size_t>(g) * a.d_row + r] = static_cast<uint8_t>(p.z);
         }
       }
-      const int j = 32 * sub0 + k;
-      const float v = __shfl_sync(0xffffffffu, w[k], src_base | sub0);
+      const int j = CPL * seg + k;
+      const float v = __shfl_sync(0xffffffffu, w[k], src_base | seg);
       const float q = fminf(fmaxf(rintf(v * p.r) + p.z, 0.f), a.maxq);
       const float dq = p.s * (q - p.z);
       const float e = (v - dq) * inv_d[j];
-      const float* urow = urow_base + k * 4 * SEG;
+      const float* urow = urow_base + k * UROW;
 #pragma unroll
-      for (int t = 0; t < 32; t += 4) {
+      for (int t = 0; t < CPL; t += 4) {
         const float4 u4 = *reinterpret_cast<const float4*>(urow + t);
         w[t] = fmaf(-e, u4.x, w[t]);
         w[t + 1] = fmaf(-e, u4.y, w[t + 1]);
         w[t + 2] = fmaf(-e, u4.z, w[t + 2]);
         w[t + 3] = fmaf(-e, u4.w, w[t + 3]);
       }
-      if (sub == sub0) {
-        err_s[row_local * (CB + 1) + j] = e;
-        code_s[row_local * CB + j] = static_cast<uint8_t>(q);
+      // The owner lane keeps the error and code of its own columns in
+      // registers (no shared-memory stores inside the loop, so the next
+      // columns' U loads can be issued early).
+      if (sub == seg) {
+        e_own[k] = e;
+        q_own[k] = q;
       }
     }
+  }
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    err_s[row_local * (CB + 1) + CPL * sub + k] = e_own[k];
+    code_s[row_local * CB + CPL * sub + k] = static_cast<uint8_t>(q_own[k]);
   }
   __syncthreads();
   // Err block and codes (original column order) for this CTA's rows.
@@ -261,8 +280,8 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
     if (rr >= a.d_row) continue;
     float h, l;
     split_tf32(err_s[rl * (CB + 1) + c], h, l);
-    a.Err_hi[static_cast<size_t>(rr) * CB + c] = h;
-    a.Err_lo[static_cast<size_t>(rr) * CB + c] = l;
+    a.Err_hi[static_cast<size_t>(rr) * SB + a.err_col0 + c] = h;
+    a.Err_lo[static_cast<size_t>(rr) * SB + a.err_col0 + c] = l;
     a.codes[static_cast<size_t>(rr) * d + a.perm[i1 + c]] = code_s[rl * CB + c];
   }
 }
@@ -291,7 +310,7 @@ __global__ void transpose_split_kernel(const float* __restrict__ U, int d, float
 }  // namespace
 
 constexpr size_t kColumnSmem =
-    sizeof(float) * (CB * 4 * SEG + CB + CL_ROWS * (CB + 1)) + CL_ROWS * CB;
+    sizeof(float) * (CB * UROW + CB + CL_ROWS * (CB + 1)) + CL_ROWS * CB;
 
 struct QuantLayout {
   size_t status, Wf, Err_hi, Err_lo, Ut_hi, Ut_lo, total;
@@ -307,9 +326,9 @@ static QuantLayout quant_layout(int64_t d_row, int64_t d_col) {
   L.Wf = off;
   off = align256q(off + sizeof(float) * d_row * d_col);
   L.Err_hi = off;
-  off = align256q(off + sizeof(float) * d_row * CB);
+  off = align256q(off + sizeof(float) * d_row * SB);
   L.Err_lo = off;
-  off = align256q(off + sizeof(float) * d_row * CB);
+  off = align256q(off + sizeof(float) * d_row * SB);
   L.Ut_hi = off;
   off = align256q(off + sizeof(float) * d_col * d_col);
   L.Ut_lo = off;
@@ -361,42 +380,60 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
   }
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(column_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(kColumnSmem)));
-  for (int i1 = 0; i1 < d_col; i1 += CB) {
-    const int nc = std::min(CB, d_col - i1);
-    ColumnArgs ca;
-    ca.Wf = Wf;
-    ca.d_row = d_row;
-    ca.d_col = d_col;
-    ca.i1 = i1;
-    ca.ncols = nc;
-    ca.U = U;
-    ca.perm = perm;
-    ca.maxq = maxq;
-    ca.gs = gs;
-    ca.sym = cfg.sym;
-    ca.codes = codes;
-    ca.scales = scales;
-    ca.zeros = zeros;
-    ca.Err_hi = Err_hi;
-    ca.Err_lo = Err_lo;
-    column_block_kernel<<<(d_row + CL_ROWS - 1) / CL_ROWS, CL_THREADS, kColumnSmem, st>>>(ca);
-    GPTQ_LAUNCH_CHECK();
-    const int i2 = i1 + nc;
-    if (i2 < d_col) {
-      TGemmArgs g;
-      g.M = d_row;
-      g.N = d_col - i2;
-      g.K = nc;
-      g.alpha = -1.f;
-      g.beta = 1.f;
-      g.C = Wf + i2;
-      g.ldc = d_col;
-      g.lower = 0;
-      g.row_off = 0;
-      g.col_off = 0;
-      const gptq_status_t s = launch_tgemm_3xtf32(
-          Err_hi, Err_lo, CB, Ut_hi + static_cast<int64_t>(i2) * d_col + i1,
-          Ut_lo + static_cast<int64_t>(i2) * d_col + i1, d_col, g, st);
+  // Two CTAs per SM need the largest shared-memory carveout.
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(column_block_kernel,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100));
+  // Two-level lazy update: after each 128-column block only the rest of its
+  // 512-column super-block is updated; after the super-block, everything to
+  // its right is updated in one K = 512 product.  The sum is the same as the
+  // single-level schedule up to the order of fp32 additions.
+  auto trailing = [&](int k0, int k_len, int e0, int n0, int n1) -> gptq_status_t {
+    TGemmArgs g;
+    g.M = d_row;
+    g.N = n1 - n0;
+    g.K = k_len;
+    g.alpha = -1.f;
+    g.beta = 1.f;
+    g.C = Wf + n0;
+    g.ldc = d_col;
+    g.lower = 0;
+    g.row_off = 0;
+    g.col_off = 0;
+    return launch_tgemm_3xtf32(Err_hi + e0, Err_lo + e0, SB,
+                               Ut_hi + static_cast<int64_t>(n0) * d_col + k0,
+                               Ut_lo + static_cast<int64_t>(n0) * d_col + k0, d_col, g, st);
+  };
+  for (int sb0 = 0; sb0 < d_col; sb0 += SB) {
+    const int sb1 = std::min(sb0 + SB, d_col);
+    for (int i1 = sb0; i1 < sb1; i1 += CB) {
+      const int nc = std::min(CB, sb1 - i1);
+      ColumnArgs ca;
+      ca.Wf = Wf;
+      ca.d_row = d_row;
+      ca.d_col = d_col;
+      ca.i1 = i1;
+      ca.ncols = nc;
+      ca.U = U;
+      ca.perm = perm;
+      ca.maxq = maxq;
+      ca.gs = gs;
+      ca.sym = cfg.sym;
+      ca.codes = codes;
+      ca.scales = scales;
+      ca.zeros = zeros;
+      ca.Err_hi = Err_hi;
+      ca.Err_lo = Err_lo;
+      ca.err_col0 = i1 - sb0;
+      column_block_kernel<<<(d_row + CL_ROWS - 1) / CL_ROWS, CL_THREADS, kColumnSmem, st>>>(ca);
+      GPTQ_LAUNCH_CHECK();
+      const int i2 = i1 + nc;
+      if (i2 < sb1) {
+        const gptq_status_t s = trailing(i1, nc, i1 - sb0, i2, sb1);
+        if (s != GPTQ_OK) return s;
+      }
+    }
+    if (sb1 < d_col) {
+      const gptq_status_t s = trailing(sb0, sb1 - sb0, 0, sb1, d_col);
       if (s != GPTQ_OK) return s;
     }
   }

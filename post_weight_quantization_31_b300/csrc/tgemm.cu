@@ -287,8 +287,14 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
   if (!make_f32_map(&m_ahi, A_hi, args.M, args.K, lda) || !make_f32_map(&m_alo, A_lo, args.M, args.K, lda) ||
       !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb) || !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb))
     return GPTQ_ERR_CUDA;
-  GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     SMEM_BYTES));
+  static int attr_dev = -1;
+  int dev = 0;
+  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (attr_dev != dev) {
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES));
+    attr_dev = dev;
+  }
   const int grid = std::min(sm_count(), s.tiles);
   tgemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m_ahi, m_alo, m_bhi, m_blo, args, s,
                                                       fault_word_ptr());
