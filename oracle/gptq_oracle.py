@@ -83,6 +83,36 @@ def hessian_sum(X: np.ndarray) -> np.ndarray:
     return X64 @ X64.T
 
 
+def hessian_sum_chunked(X: np.ndarray, chunk: int = 16384) -> np.ndarray:
+    """The same S = X X^T in fp64, summed over chunks of tokens so that the
+    fp64 copy of X never has to exist whole (full-size layers)."""
+    d = X.shape[0]
+    S = np.zeros((d, d), dtype=np.float64)
+    for t0 in range(0, X.shape[1], chunk):
+        Xc = np.asarray(X[:, t0:t0 + chunk], dtype=np.float64)
+        S += Xc @ Xc.T
+    return S
+
+
+def hessian_diag(X: np.ndarray, chunk: int = 16384) -> np.ndarray:
+    """diag(S) = sum_t X[i, t]^2 in fp64, by token chunks."""
+    out = np.zeros(X.shape[0], dtype=np.float64)
+    for t0 in range(0, X.shape[1], chunk):
+        Xc = np.asarray(X[:, t0:t0 + chunk], dtype=np.float64)
+        out += np.einsum("ij,ij->i", Xc, Xc)
+    return out
+
+
+def hessian_columns(X: np.ndarray, cols, chunk: int = 8192) -> np.ndarray:
+    """Columns S[:, cols] = X X[cols]^T in fp64, by token chunks."""
+    cols = np.asarray(cols)
+    out = np.zeros((X.shape[0], len(cols)), dtype=np.float64)
+    for t0 in range(0, X.shape[1], chunk):
+        Xc = np.asarray(X[:, t0:t0 + chunk], dtype=np.float64)
+        out += Xc @ Xc[cols].T
+    return out
+
+
 def hessian_entry(X: np.ndarray, i: int, j: int) -> float:
     """One entry S[i, j] = sum_t X[i, t] X[j, t], computed on its own."""
     xi = np.asarray(X[i], dtype=np.float64)
@@ -109,10 +139,15 @@ def act_order(H: np.ndarray, desc_act: bool) -> np.ndarray:
     """Processing order (R2).  [G] §2.2: columns are ordered once, up front,
     by the Hessian diagonal from large to small; §3.3: desc_act switches it.
     Stable sort: equal diagonals keep their original relative order."""
-    n = H.shape[0]
+    return act_order_diag(np.diag(H), desc_act)
+
+
+def act_order_diag(hdiag: np.ndarray, desc_act: bool) -> np.ndarray:
+    """act_order from the Hessian diagonal alone."""
+    n = len(hdiag)
     if not desc_act:
         return np.arange(n, dtype=np.int64)
-    return np.argsort(-np.diag(H), kind="stable").astype(np.int64)
+    return np.argsort(-np.asarray(hdiag, dtype=np.float64), kind="stable").astype(np.int64)
 
 
 def hinv_upper(H: np.ndarray) -> np.ndarray:

@@ -12,9 +12,14 @@
 //     tile, k-slab]; both K-major, fp16 x fp16 -> fp32 in TMEM.
 //   * Operands are staged by TMA (128-byte swizzle, 64 tokens per stage)
 //     through a 4-stage mbarrier ring; one thread issues tcgen05.mma, one
-//     thread issues TMA, four warps drain the accumulator.
-//   * Two 256-column TMEM accumulators (all 512 columns): the drain of one
-//     job overlaps the MMAs of the next.
+//     thread issues TMA, eight warps drain the accumulators.
+//   * Two 256-column TMEM accumulators (all 512 columns).  The tensor cores
+//     add into an accumulator with a rounding that is biased over long
+//     chains (measured: S_ii 0.15% low after 262144 tokens), so one
+//     accumulator takes at most CH slabs (1024 tokens); eight drain warps then
+//     add it into fp32 registers with round-to-nearest while the MMAs fill
+//     the other accumulator.  A job's sum leaves the registers once, at its
+//     end.
 //   * Jobs: whole tiles with the full token range first, in waves of one
 //     tile per CTA (every CTA of a wave sweeps the tokens at the same pace,
 //     so each X slab is read from HBM about once per wave and re-served from
@@ -41,7 +46,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2-5 drain
+constexpr int NUM_THREADS = 320;    // warp 0 TMA, warp 1 MMA, warps 2-9 drain
+constexpr int CH = 16;              // slabs (BK tokens each) per accumulator fill
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
-      mbar_init(acce_bar(i), 128);
+      mbar_init(acce_bar(i), 256);
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
@@ -167,81 +173,107 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int job = blockIdx.x; ok && job < s.jobs; job += gridDim.x) {
         int ti, tj, k0, k1;
         job_of(s, job, ti, tj, k0, k1);
-        if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, fault)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = k0; kb < k1; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, fault)) {
+        for (int c0 = k0; ok && c0 < k1; c0 += CH) {
+          const int c1 = min(k1, c0 + CH);
+          if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, fault)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint64_t da = smem_desc_sw128_kmajor(sa);
-          const uint64_t db = smem_desc_sw128_kmajor(sa + A_BYTES);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+          for (int kb = c0; kb < c1; ++kb) {
+            if (!mbar_wait_bounded(full_bar(stage), phase, fault)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+            const uint64_t da = smem_desc_sw128_kmajor(sa);
+            const uint64_t db = smem_desc_sw128_kmajor(sa + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / UK; ++k) {
-            // Advance 32 bytes (16 fp16) along K inside the swizzle atom.
-            const uint64_t off = static_cast<uint64_t>((k * UK * 2) >> 4);
-            tc_mma_f16(d_tmem, da + off, db + off, idesc, (kb > k0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / UK; ++k) {
+              // Advance 32 bytes (16 fp16) along K inside the swizzle atom.
+              const uint64_t off = static_cast<uint64_t>((k * UK * 2) >> 4);
+              tc_mma_f16(d_tmem, da + off, db + off, idesc, (kb > c0 || k > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));  // frees the slot when these MMAs finish
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit(empty_bar(stage));  // frees the slot when these MMAs finish
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit(accf_bar(acc));  // accumulator ready for the drain warps
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
         }
-        if (!ok) break;
-        tc_commit(accf_bar(acc));  // accumulator ready for the drain warps
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
       // Make sure no MMA is still writing TMEM before it is released.
       tc_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, fault);
     }
   } else {
-    // ------------------------------------------------------------ drain (4 warps)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ drain (8 warps)
+    // Warp w reads TMEM lanes 32q..32q+31 (q = w mod 4, the lane quarter it
+    // may access) and columns 128h..128h+127 of the tile (h = 0 for warps
+    // 2-5, 1 for warps 6-9); each lane sums one row's 128 columns.
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     const int d = s.d;
-    for (int job = blockIdx.x; job < s.jobs; job += gridDim.x) {
+    bool ok = true;
+    for (int job = blockIdx.x; ok && job < s.jobs; job += gridDim.x) {
       int ti, tj, k0, k1;
       job_of(s, job, ti, tj, k0, k1);
-      if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) break;
-      tc_fence_after();
+      float sum[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sum[i] = 0.f;
+      for (int c0 = k0; c0 < k1; c0 += CH) {
+        if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * BN + h * 128 + c * 32),
+                             v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) sum[c * 32 + i] += v[i];
+        }
+        tc_fence_before();
+        mbar_arrive(acce_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!ok) break;
       const int r = ti * BM + q * 32 + lane;
       const int row0 = ti * BM;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int cb = tj * BN + c * 32;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cb = tj * BN + h * 128 + c * 32;
         if (cb + 31 < row0 || cb >= d) continue;  // chunk wholly below the diagonal / outside
-        float v[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(acc * BN + c * 32),
-                           v);
         if (r < d) {
           float* srow = S + static_cast<size_t>(r) * d;
           if (cb >= r) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
               atomicAdd(reinterpret_cast<float4*>(srow + cb + i),
-                        make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                        make_float4(sum[c * 32 + i], sum[c * 32 + i + 1], sum[c * 32 + i + 2],
+                                    sum[c * 32 + i + 3]));
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (cb + i >= r) atomicAdd(srow + cb + i, v[i]);
+              if (cb + i >= r) atomicAdd(srow + cb + i, sum[c * 32 + i]);
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (cb + i > r) atomicAdd(S + static_cast<size_t>(cb + i) * d + r, v[i]);
+            if (cb + i > r) atomicAdd(S + static_cast<size_t>(cb + i) * d + r, sum[c * 32 + i]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(acce_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
   }
 

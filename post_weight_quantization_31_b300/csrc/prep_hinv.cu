@@ -103,10 +103,15 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int d) {
 // ---------------------------------------------------------------- gather
 // Z[i][j] = (2/n) S[q(i)][q(j)] + lambda [i == j] for i >= j, q(i) = perm[d-1-i];
 // also U[i][j] = 0 for i > j (the part of U the panel steps do not write).
-__global__ void prep_gather_kernel(const float* __restrict__ S, const int32_t* __restrict__ perm, int d,
-                                   float hscale, const float* __restrict__ lam,
-                                   float* __restrict__ Z, float* __restrict__ U,
-                                   int* __restrict__ status) {
+// With the fp64 diagonal given, the diagonal of H is taken from it: the
+// tensor-core sums of S are biased low on the diagonal, where every term is
+// positive (about 5e-6 relative per 1024-token accumulator fill), and that
+// bias alone moves U by about 1e-6 at d_col = 13824.
+__global__ void prep_gather_kernel(const float* __restrict__ S, const double* __restrict__ diag,
+                                   const int32_t* __restrict__ perm, int d, float hscale,
+                                   double hscale_d, const float* __restrict__ lam,
+                                   float* __restrict__ Z, float* __restrict__ zlo,
+                                   float* __restrict__ U, int* __restrict__ status) {
   const int bi = blockIdx.y, bj = blockIdx.x;
   if (bj > bi) return;
   const int i = bi * 32 + threadIdx.y * 4;
@@ -122,7 +127,13 @@ __global__ void prep_gather_kernel(const float* __restrict__ S, const int32_t* _
       const int qi = perm[d - 1 - ii];
       const int a = max(qi, qj), b = min(qi, qj);
       float v = S[static_cast<size_t>(a) * d + b] * hscale;
-      if (ii == j) v += l;
+      if (ii == j) {
+        // The diagonal is carried as Z + zlo (see the update GEMM).
+        const double v64 = (diag ? diag[qi] : static_cast<double>(S[static_cast<size_t>(a) * d + b])) *
+                               hscale_d + static_cast<double>(l);
+        v = static_cast<float>(v64);
+        zlo[ii] = static_cast<float>(v64 - static_cast<double>(v));
+      }
       if (!isfinite(v)) bad = 1;
       Z[static_cast<size_t>(ii) * d + j] = v;
       if (ii > j) U[static_cast<size_t>(ii) * d + j] = 0.f;
@@ -145,6 +156,7 @@ struct PanelArgs {
   float* Blo;
   float* U;       // [n][n] output
   int* status;
+  const float* zlo;  // [n] low parts of the diagonal of Z
 };
 
 __device__ __forceinline__ void store_split(float* hi, float* lo, int64_t off, float v) {
@@ -189,9 +201,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 // Returns true (in thread 0) if a pivot was not positive.
 constexpr int TMLD = 36;  // row stride of the 32 x 32 level products
 
-__device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, int k, int b,
+__device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* __restrict__ zlo,
+                                      int64_t ldz, int k, int b,
                                       float* __restrict__ Mt, float* __restrict__ Ls,
-                                      float* __restrict__ rinv, float* __restrict__ Tm,
+                                      float* __restrict__ ldiag, float* __restrict__ Tm,
                                       float* __restrict__ LT, float* __restrict__ colbuf) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int nsub = b >> 5;
@@ -199,6 +212,13 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
     const int i = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (i < b && c4 <= i) v = *reinterpret_cast<const float4*>(Z + static_cast<int64_t>(k + i) * ldz + k + c4);
+    if (i < b && c4 <= i && i < c4 + 4) {  // the diagonal element, hi + lo
+      const float lo = zlo[k + i];
+      if (i == c4) v.x += lo;
+      else if (i == c4 + 1) v.y += lo;
+      else if (i == c4 + 2) v.z += lo;
+      else v.w += lo;
+    }
     *reinterpret_cast<float4*>(Ls + i * LDM + c4) = v;
     *reinterpret_cast<float4*>(Mt + i * LDM + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -221,7 +241,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         if (c > lane) a[c] = 0.f;
-      float my_r = 1.f;
+      float my_l = 1.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float ajj = __shfl_sync(0xffffffffu, a[j], j);
@@ -229,9 +249,9 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
           bad = true;
           ajj = 1.f;
         }
-        const float r = rsqrtf(ajj);  // 1 / l_jj
-        if (lane == j) my_r = r;
-        const float l = (lane == j) ? ajj * r : a[j] * r;  // l_ij for lanes i >= j
+        const float ljj = sqrtf(ajj);  // correctly rounded, as is the division below
+        if (lane == j) my_l = ljj;
+        const float l = (lane == j) ? ljj : __fdiv_rn(a[j], ljj);  // l_ij for lanes i >= j
         a[j] = (lane >= j) ? l : 0.f;
         // column j of L to every lane (double-buffered: one warp barrier per column)
         float* cb = colbuf + (j & 1) * 32;
@@ -251,7 +271,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
         *reinterpret_cast<float4*>(row + c) =
             make_float4(c <= lane ? a[c] : 0.f, c + 1 <= lane ? a[c + 1] : 0.f,
                         c + 2 <= lane ? a[c + 2] : 0.f, c + 3 <= lane ? a[c + 3] : 0.f);
-      rinv[c0 + lane] = my_r;
+      ldiag[c0 + lane] = my_l;
     }
     __syncthreads();
     // ---- T: rows below the sub-block, within the diagonal block
@@ -268,7 +288,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float x = a[c] * rinv[c0 + c];
+        const float x = __fdiv_rn(a[c], ldiag[c0 + c]);
         a[c] = x;
 #pragma unroll
         for (int m = c + 1; m < 32; ++m) a[m] = fmaf(-x, Ls[(c0 + m) * LDM + c0 + c], a[m]);
@@ -329,7 +349,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, int64_t ldz, 
     for (int c = 0; c < 32; ++c) acc[c] = (c == lane) ? 1.f : 0.f;
 #pragma unroll
     for (int m = 31; m >= 0; --m) {
-      const float ym = (m <= lane) ? acc[m] * rinv[w0 + m] : 0.f;
+      const float ym = (m <= lane) ? __fdiv_rn(acc[m], ldiag[w0 + m]) : 0.f;
       y[m] = ym;
 #pragma unroll
       for (int c = 0; c < m; ++c) acc[c] = fmaf(-ym, Ls[(w0 + m) * LDM + w0 + c], acc[c]);
@@ -393,8 +413,8 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
   float* Ls = T + NB * LDM;          // [NB][LDM]  diagonal block, then L_kk
-  float* rinv = Ls + NB * LDM;       // [NB]       1 / diag(L_kk)
-  float* Tm = rinv + NB;             // [3][32][TMLD] level products
+  float* ldiag = Ls + NB * LDM;       // [NB]       diag(L_kk)
+  float* Tm = ldiag + NB;             // [3][32][TMLD] level products
   float* LT = Tm;                    // [32][LDM] transposed sub-panel (shares Tm's space)
   float* colbuf = LT + 32 * LDM;     // [2][32]
   const int n = p.n, k = p.k, b = p.b;
@@ -423,7 +443,7 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
-  const bool notpd = factor_invert_blocked(p.Z, ldz, k, b, Mt, Ls, rinv, Tm, LT, colbuf);
+  const bool notpd = factor_invert_blocked(p.Z, p.zlo, ldz, k, b, Mt, Ls, ldiag, Tm, LT, colbuf);
   if (role == 0 && t == 0 && notpd) atomicOr(p.status, kStatNotPD);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
@@ -518,7 +538,7 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct PrepLayout {
-  size_t status, lam, keys, Z, Bhi, Blo, total;
+  size_t status, lam, keys, zlo, Z, Bhi, Blo, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -532,6 +552,8 @@ static PrepLayout prep_layout(int64_t d) {
   off += 256;
   L.keys = off;
   off = align256(off + sizeof(unsigned long long) * d);
+  L.zlo = off;
+  off = align256(off + sizeof(float) * d);
   L.Z = off;
   off = align256(off + sizeof(float) * d * d);
   L.Bhi = off;
@@ -554,6 +576,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   float* lam = reinterpret_cast<float*>(base + L.lam);
   auto* keys = reinterpret_cast<unsigned long long*>(base + L.keys);
   float* Z = reinterpret_cast<float*>(base + L.Z);
+  float* zlo = reinterpret_cast<float*>(base + L.zlo);
   float* Bhi = reinterpret_cast<float*>(base + L.Bhi);
   float* Blo = reinterpret_cast<float*>(base + L.Blo);
   const double hscale = 2.0 / static_cast<double>(n_seen);
@@ -569,8 +592,8 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   GPTQ_LAUNCH_CHECK();
   {
     dim3 grid((d + 31) / 32, (d + 31) / 32), block(32, 8);
-    prep_gather_kernel<<<grid, block, 0, st>>>(S, perm, d, static_cast<float>(hscale), lam, Z, U,
-                                                status);
+    prep_gather_kernel<<<grid, block, 0, st>>>(S, diag, perm, d, static_cast<float>(hscale), hscale, lam,
+                                                Z, zlo, U, status);
     GPTQ_LAUNCH_CHECK();
   }
   const size_t smem = sizeof(float) * (3 * NB * LDM + NB + 32 * LDM + 64);
@@ -588,6 +611,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     pa.Blo = Blo;
     pa.U = U;
     pa.status = status;
+    pa.zlo = zlo;
     const int n_pan = (d - k - b + NB - 1) / NB;
     panel_step_kernel<<<1 + pa.n_acc + n_pan, PT, smem, st>>>(pa);
     GPTQ_LAUNCH_CHECK();
@@ -603,6 +627,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
       g.lower = 1;
       g.row_off = k + b;
       g.col_off = 0;
+      g.diag_lo = zlo;
       const gptq_status_t s = launch_tgemm_3xtf32(Bhi + static_cast<int64_t>(k + b) * NB,
                                                   Blo + static_cast<int64_t>(k + b) * NB, NB, Bhi, Blo,
                                                   NB, g, st);

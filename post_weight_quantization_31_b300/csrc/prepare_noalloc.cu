@@ -20,9 +20,10 @@ namespace {
 constexpr int64_t kMaxDCol = GPTQ_NOALLOC_MAX_D_COL;
 constexpr size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Room for the prepare workspace at d_col = kMaxDCol: status and damping
-// words, the 64-bit sort keys, the d x d work matrix and the two d x 128
-// panel operands.  launch time checks it against prep_workspace_bytes().
-constexpr size_t kScratchBytes = 256 + 256 + round256(8 * kMaxDCol) +
+// words, the 64-bit sort keys, the low parts of the work matrix's diagonal,
+// the d x d work matrix and the two d x 128 panel operands.  Each call
+// checks it against prep_workspace_bytes().
+constexpr size_t kScratchBytes = 256 + 256 + round256(8 * kMaxDCol) + round256(4 * kMaxDCol) +
                                  round256(4 * kMaxDCol * kMaxDCol) + 2 * round256(4 * kMaxDCol * 128);
 
 static __device__ __align__(256) unsigned char g_prep_scratch[kScratchBytes];

@@ -189,6 +189,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            v);
         if (!row_ok) continue;
         const bool full = (n0 + 32 <= a.N) && (!a.lower || n0 + 31 <= diag);
+        if (a.diag_lo && row_ok && diag >= n0 && diag < n0 + 32 && diag < a.N) {
+          // the diagonal element of this row lies in the chunk: two-sum
+          const int i = static_cast<int>(diag - n0);
+          const float cv = crow[diag];
+          const float t = -v[i];
+          const float sum = cv + t;
+          const float bb = sum - cv;
+          const float err = (cv - (sum - bb)) + (t - bb);
+          a.diag_lo[a.col_off + diag] += err;
+        }
         if (full && (a.ldc % 4 == 0)) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {

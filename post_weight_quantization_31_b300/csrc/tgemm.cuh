@@ -4,7 +4,7 @@
 //
 // A [M, K] and B [N, K] are row-major (K contiguous, "K-major") and each is
 // given as two fp32 arrays hi + lo with hi exactly representable in TF32
-// (10-bit mantissa) and lo = x - hi; see split_tf32().  The product is
+// (10-bit mantissa) and lo ~ x - hi; see split_tf32().  The product is
 // formed as A_lo B_hi + A_hi B_lo + A_hi B_hi with fp32 accumulation in
 // TMEM, which keeps about 2^-21 relative accuracy per product (the dropped
 // A_lo B_lo term is ~2^-22).  With `lower`, only elements with
@@ -26,15 +26,25 @@ struct TGemmArgs {
   int64_t ldc;
   int lower;
   int row_off, col_off;
+  // Optional, with lower = 1, alpha = -1, beta = 1: for the elements on the
+  // diagonal (row_off + m == col_off + n), the exact rounding error of the
+  // update (Knuth two-sum) is added to diag_lo[col_off + n], so that
+  // C + diag_lo carries the running diagonal to about twice fp32 precision.
+  float* diag_lo = nullptr;
 };
 
 // hi: x rounded to a TF32 value (10 explicit mantissa bits, ties away);
-// lo: x - hi, exact in fp32.
-__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+// lo: x - hi rounded the same way (|x - hi - lo| <= 2^-22 |x|).
+__device__ __forceinline__ float round_tf32(float x) {
   const uint32_t u = __float_as_uint(x);
-  hi = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
-  if (!isfinite(hi)) hi = __uint_as_float(u & 0xFFFFE000u);
-  lo = __fsub_rn(x, hi);
+  const float r = __uint_as_float((u + 0x1000u) & 0xFFFFE000u);
+  return isfinite(r) ? r : __uint_as_float(u & 0xFFFFE000u);
+}
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  hi = round_tf32(x);
+  // The tensor cores read only the TF32 bits of lo; rounding it here (rather
+  // than letting the low bits be dropped) halves what the pair leaves out.
+  lo = round_tf32(__fsub_rn(x, hi));
 }
 
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda,

@@ -212,3 +212,30 @@ def mlp_7b(which: str, seed: int = 1003, n_tok: int = 262144,
     else:
         raise ValueError(which)
     return LayerInputs(f"mlp_{which}", W, "bf16", X, CFG_7B_MLP)
+
+
+def decoder_site_7b(site: str, layer: int = 0, n_tok: int = 65536) -> LayerInputs:
+    """One input site of a 7B-shaped decoder layer (the 32-layer set): the
+    matrices that read the same activations share one X, so their rows are
+    stacked into one W.  site: "qkv" (3 x 4096 rows, d_col 4096), "o"
+    (4096 x 4096), "gate_up" (2 x 11008 rows, d_col 4096), "down"
+    (4096 x 11008).  X: N(0,1) with 1% of channels x U[10,50]; 4-bit sym g128."""
+    shapes = {"qkv": (3 * 4096, 4096), "o": (4096, 4096), "gate_up": (2 * 11008, 4096),
+              "down": (4096, 11008)}
+    d_row, d_col = shapes[site]
+    seed = 1004 + 100 * layer + {"qkv": 0, "o": 10, "gate_up": 20, "down": 30}[site]
+    W = make_weight(d_row, d_col, seed, dtype="bf16")
+    X = make_activations(d_col, n_tok, seed + 1, outlier_frac=0.01, outlier_scale=(10.0, 50.0))
+    return LayerInputs(f"decoder{layer}_{site}", W, "bf16", X, CFG_7B_SET)
+
+
+def lowbit_13b(which: str, bits: int, n_tok: int = 131072) -> LayerInputs:
+    """13B-shaped low-bit sweep: "attn" 5120x5120, "gate_up" 2 x 13824 rows
+    x 5120 (one shared X), "down" 5120 x 13824.  X: N(0,1) with 1% of
+    channels x U[10,50]; bits 3 or 2, sym, g64, damp 0.1, desc_act on."""
+    shapes = {"attn": (5120, 5120), "gate_up": (2 * 13824, 5120), "down": (5120, 13824)}
+    d_row, d_col = shapes[which]
+    seed = 1005 + {"attn": 0, "gate_up": 10, "down": 20}[which]
+    W = make_weight(d_row, d_col, seed, dtype="bf16")
+    X = make_activations(d_col, n_tok, seed + 1, outlier_frac=0.01, outlier_scale=(10.0, 50.0))
+    return LayerInputs(f"lowbit13b_{which}_{bits}bit", W, "bf16", X, cfg_13b_lowbit(bits))

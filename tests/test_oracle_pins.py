@@ -251,3 +251,22 @@ def test_hessian_entry_matches_sum():
     assert S[3, 7] == O.hessian_entry(X, 3, 7)
     Xf = X.astype(np.float64)
     assert S[5, 5] == sum(float(v) * float(v) for v in Xf[5])
+
+
+def test_chunked_hessian_helpers_match_brute_force():
+    """The chunked fp64 sums used at full size against explicit Python loops."""
+    X = wl.make_activations(12, 50, seed=82, n_outliers=2, outlier_scale=20.0)
+    Xf = [[float(v) for v in row] for row in X]
+    brute = np.array([[sum(a * b for a, b in zip(Xf[i], Xf[j])) for j in range(12)]
+                      for i in range(12)])
+    np.testing.assert_allclose(O.hessian_sum_chunked(X, chunk=7), brute, rtol=1e-12, atol=0)
+    np.testing.assert_allclose(O.hessian_diag(X, chunk=9), np.diag(brute), rtol=1e-12, atol=0)
+    np.testing.assert_allclose(O.hessian_columns(X, [3, 0, 11], chunk=13), brute[:, [3, 0, 11]],
+                               rtol=1e-12, atol=0)
+
+
+def test_act_order_from_diagonal():
+    d = np.array([1.0, 3.0, 3.0, 0.5, 2.0])
+    assert list(O.act_order_diag(d, True)) == [1, 2, 4, 0, 3]   # tie keeps 1 before 2
+    assert list(O.act_order_diag(d, False)) == [0, 1, 2, 3, 4]
+    assert list(O.act_order(np.diag(d), True)) == [1, 2, 4, 0, 3]
