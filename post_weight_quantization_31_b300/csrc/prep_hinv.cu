@@ -101,22 +101,38 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int d) {
 }
 
 // ---------------------------------------------------------------- gather
-// Z[i][j] = (2/n) S[q(i)][q(j)] + lambda [i == j] for i >= j, q(i) = perm[d-1-i];
-// also U[i][j] = 0 for i > j (the part of U the panel steps do not write).
-// With the fp64 diagonal given, the diagonal of H is taken from it: the
-// tensor-core sums of S are biased low on the diagonal, where every term is
-// positive (about 5e-6 relative per 1024-token accumulator fill), and that
-// bias alone moves U by about 1e-6 at d_col = 13824.
-__global__ void prep_gather_kernel(const float* __restrict__ S, const double* __restrict__ diag,
-                                   const int32_t* __restrict__ perm, int d, float hscale,
-                                   double hscale_d, const float* __restrict__ lam,
-                                   float* __restrict__ Z, float* __restrict__ zlo,
-                                   float* __restrict__ U, int* __restrict__ status) {
+// prep_diag_kernel: Z[i][i] + zlo[i] = (2/n) S_ii + lambda, formed in fp64 and
+// carried as an fp32 pair (see the update GEMM), S_ii taken from the fp64
+// diagonal when it is given: the tensor-core sums of S are biased low on the
+// diagonal, where every term is positive (about 5e-6 relative per
+// 1024-token accumulator fill), and that bias alone moves U by about 1e-6 at
+// d_col = 13824.
+// prep_gather_kernel: Z[i][j] = (2/n) S[q(i)][q(j)] for i > j, with
+// q(i) = perm[d-1-i]; also U[i][j] = 0 for i > j (the part of U the panel
+// steps do not write).
+__global__ void prep_diag_kernel(const float* __restrict__ S, const double* __restrict__ diag,
+                                 const int32_t* __restrict__ perm, int d, double hscale_d,
+                                 const float* __restrict__ lam, float* __restrict__ Z,
+                                 float* __restrict__ zlo, int* __restrict__ status) {
+  // The diagonal is carried as Z + zlo (see the update GEMM).
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  const int qi = perm[d - 1 - i];
+  const double s = diag ? diag[qi] : static_cast<double>(S[static_cast<size_t>(qi) * d + qi]);
+  const double v64 = s * hscale_d + static_cast<double>(*lam);
+  const float v = static_cast<float>(v64);
+  Z[static_cast<size_t>(i) * d + i] = v;
+  zlo[i] = static_cast<float>(v64 - static_cast<double>(v));
+  if (!isfinite(v)) atomicOr(status, kStatNonFinite);
+}
+
+__global__ void prep_gather_kernel(const float* __restrict__ S, const int32_t* __restrict__ perm, int d,
+                                   float hscale, float* __restrict__ Z, float* __restrict__ U,
+                                   int* __restrict__ status) {
   const int bi = blockIdx.y, bj = blockIdx.x;
   if (bj > bi) return;
   const int i = bi * 32 + threadIdx.y * 4;
   const int j = bj * 32 + threadIdx.x;
-  const float l = *lam;
   int bad = 0;
   if (j < d) {
     const int qj = perm[d - 1 - j];
@@ -126,14 +142,8 @@ __global__ void prep_gather_kernel(const float* __restrict__ S, const double* __
       if (ii >= d || j > ii) continue;
       const int qi = perm[d - 1 - ii];
       const int a = max(qi, qj), b = min(qi, qj);
-      float v = S[static_cast<size_t>(a) * d + b] * hscale;
-      if (ii == j) {
-        // The diagonal is carried as Z + zlo (see the update GEMM).
-        const double v64 = (diag ? diag[qi] : static_cast<double>(S[static_cast<size_t>(a) * d + b])) *
-                               hscale_d + static_cast<double>(l);
-        v = static_cast<float>(v64);
-        zlo[ii] = static_cast<float>(v64 - static_cast<double>(v));
-      }
+      if (ii == j) continue;  // the diagonal: prep_diag_kernel
+      const float v = S[static_cast<size_t>(a) * d + b] * hscale;
       if (!isfinite(v)) bad = 1;
       Z[static_cast<size_t>(ii) * d + j] = v;
       if (ii > j) U[static_cast<size_t>(ii) * d + j] = 0.f;
@@ -143,8 +153,7 @@ __global__ void prep_gather_kernel(const float* __restrict__ S, const double* __
 }
 
 // ---------------------------------------------------------------- panel step
-constexpr int PT = 512;   // threads per panel CTA: thread t owns rows 4(t>>4)..+3,
-                          // columns 8(t&15)..+7 of a 128 x 128 block
+constexpr int PT = 512;   // threads per panel CTA
 constexpr int LDM = NB + 4;  // padded row (16-byte aligned rows)
 
 struct PanelArgs {
@@ -157,6 +166,7 @@ struct PanelArgs {
   float* U;       // [n][n] output
   int* status;
   const float* zlo;  // [n] low parts of the diagonal of Z
+  int split;         // CTAs per role tile (1, 2 or 4)
 };
 
 __device__ __forceinline__ void store_split(float* hi, float* lo, int64_t off, float v) {
@@ -201,11 +211,14 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 // Returns true (in thread 0) if a pivot was not positive.
 constexpr int TMLD = 36;  // row stride of the 32 x 32 level products
 
+constexpr int LST = 36;  // row stride of the transposed 32 x 32 diagonal sub-block
+
 __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* __restrict__ zlo,
                                       int64_t ldz, int k, int b,
                                       float* __restrict__ Mt, float* __restrict__ Ls,
-                                      float* __restrict__ ldiag, float* __restrict__ Tm,
-                                      float* __restrict__ LT, float* __restrict__ colbuf) {
+                                      float* __restrict__ rdiag, float* __restrict__ Tm,
+                                      float* __restrict__ LT, float* __restrict__ colbuf,
+                                      float* __restrict__ LssT) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int nsub = b >> 5;
   for (int q = t; q < NB * (NB / 4); q += PT) {
@@ -241,18 +254,22 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         if (c > lane) a[c] = 0.f;
-      float my_l = 1.f;
+      float my_r = 1.f;
+      float pn = a[0];  // lane j's current diagonal when column j starts
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float ajj = __shfl_sync(0xffffffffu, a[j], j);
+        float ajj = __shfl_sync(0xffffffffu, pn, j);
         if (!(ajj > 0.f)) {
           bad = true;
           ajj = 1.f;
         }
-        const float ljj = sqrtf(ajj);  // correctly rounded, as is the division below
-        if (lane == j) my_l = ljj;
-        const float l = (lane == j) ? ljj : __fdiv_rn(a[j], ljj);  // l_ij for lanes i >= j
+        const float r = rsqrtf(ajj);  // 1 / l_jj
+        if (lane == j) my_r = r;
+        const float l = (lane == j) ? ajj * r : a[j] * r;  // l_ij for lanes i >= j
         a[j] = (lane >= j) ? l : 0.f;
+        // Lane j+1's next pivot is its own a[j+1] - l^2: formed here, it does
+        // not wait for the broadcast below (the same fma the update does).
+        if (j + 1 < 32) pn = fmaf(-l, l, a[j + 1]);
         // column j of L to every lane (double-buffered: one warp barrier per column)
         float* cb = colbuf + (j & 1) * 32;
         cb[lane] = l;
@@ -271,7 +288,9 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
         *reinterpret_cast<float4*>(row + c) =
             make_float4(c <= lane ? a[c] : 0.f, c + 1 <= lane ? a[c + 1] : 0.f,
                         c + 2 <= lane ? a[c + 2] : 0.f, c + 3 <= lane ? a[c + 3] : 0.f);
-      ldiag[c0 + lane] = my_l;
+      rdiag[c0 + lane] = my_r;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) LssT[c * LST + lane] = (c <= lane) ? a[c] : 0.f;
     }
     __syncthreads();
     // ---- T: rows below the sub-block, within the diagonal block
@@ -288,10 +307,17 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float x = __fdiv_rn(a[c], ldiag[c0 + c]);
+        const float x = a[c] * rdiag[c0 + c];
         a[c] = x;
+        // column c of L_ss, read as rows of its transpose (broadcast loads)
 #pragma unroll
-        for (int m = c + 1; m < 32; ++m) a[m] = fmaf(-x, Ls[(c0 + m) * LDM + c0 + c], a[m]);
+        for (int m4 = (c + 1) & ~3; m4 < 32; m4 += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(LssT + c * LST + m4);
+          const float lv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (m4 + e > c) a[m4 + e] = fmaf(-x, lv[e], a[m4 + e]);
+        }
       }
 #pragma unroll
       for (int c = 0; c < 32; c += 4)
@@ -349,7 +375,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
     for (int c = 0; c < 32; ++c) acc[c] = (c == lane) ? 1.f : 0.f;
 #pragma unroll
     for (int m = 31; m >= 0; --m) {
-      const float ym = (m <= lane) ? __fdiv_rn(acc[m], ldiag[w0 + m]) : 0.f;
+      const float ym = (m <= lane) ? acc[m] * rdiag[w0 + m] : 0.f;
       y[m] = ym;
 #pragma unroll
       for (int c = 0; c < m; ++c) acc[c] = fmaf(-ym, Ls[(w0 + m) * LDM + w0 + c], acc[c]);
@@ -408,42 +434,142 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
   return bad;
 }
 
+// Role products, RT = 1, 2 or 4 rows of the output per thread: lanes take
+// the rows (lane + 32 i), warps take 8 output columns each (16 x 8 = 128).
+//   X role: X_k[r][cb + c] = sum_q M[r][q] Acc[q][cb + c], r in this CTA's rows;
+//   P role: P[rr][c] = sum_q A[rr][q] M[c][q], rr in this CTA's rows.
+template <int RT>
+__device__ __forceinline__ void role_products(const PanelArgs& p, bool xrole, int tile, int part,
+                                              const float* __restrict__ Mt,
+                                              const float* __restrict__ T) {
+  const int n = p.n, k = p.k, b = p.b;
+  const int64_t ldz = n;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = 8 * warp;
+  const int rows = 32 * RT;            // output rows of this CTA
+  const int row0 = part * rows;        // first of them within the 128-row tile
+  float acc[RT][8];
+#pragma unroll
+  for (int i = 0; i < RT; ++i)
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) acc[i][cc] = 0.f;
+  if (xrole) {
+    // Mt[q][r] = M[r][q] is zero for q > r, so q stops at the last row.
+    const int cbase = tile * NB;
+    const int qmax = min(b, row0 + rows);
+    for (int q = 0; q < qmax; ++q) {
+      const float4 t0 = *reinterpret_cast<const float4*>(T + q * LDM + c0);
+      const float4 t1 = *reinterpret_cast<const float4*>(T + q * LDM + c0 + 4);
+      const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+      for (int i = 0; i < RT; ++i) {
+        const float m = Mt[q * LDM + row0 + lane + 32 * i];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) acc[i][cc] = fmaf(m, tv[cc], acc[i][cc]);
+      }
+    }
+    const int w = min(NB, k - cbase);
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+      const int r = row0 + lane + 32 * i;
+      if (r >= b) continue;
+      float* urow = p.U + static_cast<int64_t>(n - 1 - (k + r)) * n + (n - 1 - cbase);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        if (c0 + cc >= w) continue;
+        urow[-(c0 + cc)] = acc[i][cc];
+        store_split(p.Bhi, p.Blo, static_cast<int64_t>(cbase + c0 + cc) * NB + r, acc[i][cc]);
+      }
+    }
+  } else {
+    // Mt[q][c] = M[c][q] is zero for q > c, so q stops after this warp's columns.
+    const int rbase = k + b + tile * NB + row0;   // first panel row of this CTA
+    const int h = min(rows, n - rbase);
+    const int qmax = min(b, c0 + 8);
+    for (int q = 0; q < qmax; q += 4) {
+      float4 a4[RT];
+#pragma unroll
+      for (int i = 0; i < RT; ++i) a4[i] = *reinterpret_cast<const float4*>(T + (lane + 32 * i) * LDM + q);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 m0 = *reinterpret_cast<const float4*>(Mt + (q + e) * LDM + c0);
+        const float4 m1 = *reinterpret_cast<const float4*>(Mt + (q + e) * LDM + c0 + 4);
+        const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+        for (int i = 0; i < RT; ++i) {
+          const float av = e == 0 ? a4[i].x : e == 1 ? a4[i].y : e == 2 ? a4[i].z : a4[i].w;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) acc[i][cc] = fmaf(av, mv[cc], acc[i][cc]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < RT; ++i) {
+      const int rr = lane + 32 * i;
+      if (rr >= h) continue;
+      const int64_t off = static_cast<int64_t>(rbase + rr) * NB + c0;
+      store_split4(p.Bhi, p.Blo, off, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+      store_split4(p.Bhi, p.Blo, off + 4, make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
+    }
+    // this CTA's rows of the panel become the (zero) start of the Acc columns of block k
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < h * (NB / 4); idx += PT) {
+      const int rr = idx / (NB / 4), c4 = (idx % (NB / 4)) * 4;
+      if (c4 < b)
+        *reinterpret_cast<float4*>(p.Z + static_cast<int64_t>(rbase + rr) * ldz + k + c4) =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// One step k of the factorization.  CTA 0 writes the diagonal block of U and
+// of B; the other CTAs each take `split` consecutive parts (128/split rows)
+// of one role tile: the Acc tiles left of the diagonal block (X role), then
+// the panel tiles below it (P role).  Every CTA factors the diagonal block
+// itself, while its role operand is fetched.
 __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   extern __shared__ __align__(16) float sm[];
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
   float* Ls = T + NB * LDM;          // [NB][LDM]  diagonal block, then L_kk
-  float* ldiag = Ls + NB * LDM;       // [NB]       diag(L_kk)
-  float* Tm = ldiag + NB;             // [3][32][TMLD] level products
+  float* rdiag = Ls + NB * LDM;      // [NB]       1 / diag(L_kk)
+  float* Tm = rdiag + NB;            // [3][32][TMLD] level products
   float* LT = Tm;                    // [32][LDM] transposed sub-panel (shares Tm's space)
   float* colbuf = LT + 32 * LDM;     // [2][32]
+  float* LssT = colbuf + 64;         // [32][LST] transposed diagonal sub-block
   const int n = p.n, k = p.k, b = p.b;
   const int64_t ldz = n;
-  const int t = threadIdx.x, rg = t >> 4, cg = t & 15;
-  const int r0 = 4 * rg, c0 = 8 * cg;
+  const int t = threadIdx.x;
   const int role = blockIdx.x;
+  const int tile = role >= 1 ? (role - 1) / p.split : 0;
+  const int part = role >= 1 ? (role - 1) % p.split : 0;
+  const bool xrole = role >= 1 && tile < p.n_acc;
+  const int ptile = tile - p.n_acc;  // P role: panel tile index
+  const int prow = NB / p.split;     // rows of the P operand this CTA needs
 
   // Role operand tile, fetched while the diagonal block is factored.
   if (role >= 1) {
-    const bool acc = role <= p.n_acc;
-    const int base = acc ? (role - 1) * NB : k + b + (role - 1 - p.n_acc) * NB;
-    for (int q = t; q < NB * (NB / 4); q += PT) {
-      const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
-      const float* src;
-      bool ok;
-      if (acc) {  // T[q][cc] = Acc[k + q][base + cc]
-        ok = rr < b && base + c4 < k;
-        src = p.Z + static_cast<int64_t>(k + rr) * ldz + base + c4;
-      } else {    // T[rr][q] = A[base + rr][k + q]
-        ok = base + rr < n && c4 < b;
-        src = p.Z + static_cast<int64_t>(base + rr) * ldz + k + c4;
+    if (xrole) {  // T[q][cc] = Acc[k + q][cbase + cc], all 128 q
+      const int cbase = tile * NB;
+      for (int q = t; q < NB * (NB / 4); q += PT) {
+        const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
+        const bool ok = rr < b && cbase + c4 < k;
+        const float* src = p.Z + static_cast<int64_t>(k + rr) * ldz + cbase + c4;
+        cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
       }
-      cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
+    } else {      // T[rr][q] = A[rbase + rr][k + q], this CTA's rows only
+      const int rbase = k + b + ptile * NB + part * prow;
+      for (int q = t; q < prow * (NB / 4); q += PT) {
+        const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
+        const bool ok = rbase + rr < n && c4 < b;
+        const float* src = p.Z + static_cast<int64_t>(rbase + rr) * ldz + k + c4;
+        cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
+      }
     }
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
 
-  const bool notpd = factor_invert_blocked(p.Z, p.zlo, ldz, k, b, Mt, Ls, ldiag, Tm, LT, colbuf);
+  const bool notpd = factor_invert_blocked(p.Z, p.zlo, ldz, k, b, Mt, Ls, rdiag, Tm, LT, colbuf, LssT);
   if (role == 0 && t == 0 && notpd) atomicOr(p.status, kStatNotPD);
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
@@ -462,76 +588,12 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
     }
     return;
   }
-  float acc[4][8];
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) acc[ii][cc] = 0.f;
-
-  if (role <= p.n_acc) {
-    // X_k[r][cbase + cc] = sum_q M[r][q] Acc[q][cc] = sum_q Mt[q][r] T[q][cc]
-    const int cbase = (role - 1) * NB;
-    const int qmax = min(b, r0 + 4);  // M[r][q] = 0 for q > r
-    for (int q = 0; q < qmax; ++q) {
-      const float4 m4 = *reinterpret_cast<const float4*>(Mt + q * LDM + r0);
-      const float4 t0 = *reinterpret_cast<const float4*>(T + q * LDM + c0);
-      const float4 t1 = *reinterpret_cast<const float4*>(T + q * LDM + c0 + 4);
-      const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-      const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) acc[ii][cc] = fmaf(mv[ii], tv[cc], acc[ii][cc]);
-    }
-    const int w = min(NB, k - cbase);
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-      const int r = r0 + ii;
-      if (r >= b) continue;
-      float* urow = p.U + static_cast<int64_t>(n - 1 - (k + r)) * n + (n - 1 - cbase);
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        if (c0 + cc < w) urow[-(c0 + cc)] = acc[ii][cc];
-    }
-#pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-      if (c0 + cc >= w) continue;
-      store_split4(p.Bhi, p.Blo, static_cast<int64_t>(cbase + c0 + cc) * NB + r0,
-                   make_float4(acc[0][cc], acc[1][cc], acc[2][cc], acc[3][cc]));
-    }
-  } else {
-    // P[rr][c] = sum_q A[rr][q] M[c][q] = sum_q T[rr][q] Mt[q][c]; zero the panel.
-    const int rbase = k + b + (role - 1 - p.n_acc) * NB;
-    const int h = min(NB, n - rbase);
-    const int qmax = min(b, c0 + 8);  // Mt[q][c] = 0 for q > c
-    for (int q = 0; q < qmax; ++q) {
-      const float4 m0 = *reinterpret_cast<const float4*>(Mt + q * LDM + c0);
-      const float4 m1 = *reinterpret_cast<const float4*>(Mt + q * LDM + c0 + 4);
-      const float mv[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-      float av[4];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) av[ii] = T[(r0 + ii) * LDM + q];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) acc[ii][cc] = fmaf(av[ii], mv[cc], acc[ii][cc]);
-    }
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-      const int rr = r0 + ii;
-      if (rr >= h) continue;
-      const int64_t off = static_cast<int64_t>(rbase + rr) * NB + c0;
-      store_split4(p.Bhi, p.Blo, off, make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]));
-      store_split4(p.Bhi, p.Blo, off + 4, make_float4(acc[ii][4], acc[ii][5], acc[ii][6], acc[ii][7]));
-    }
-    // the panel becomes the (zero) start of the Acc columns of block k
-    for (int idx = t; idx < h * (NB / 4); idx += PT) {
-      const int rr = idx / (NB / 4), c4 = (idx % (NB / 4)) * 4;
-      if (c4 < b)
-        *reinterpret_cast<float4*>(p.Z + static_cast<int64_t>(rbase + rr) * ldz + k + c4) =
-            make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  if (p.split == 4)
+    role_products<1>(p, xrole, xrole ? tile : ptile, part, Mt, T);
+  else if (p.split == 2)
+    role_products<2>(p, xrole, xrole ? tile : ptile, part, Mt, T);
+  else
+    role_products<4>(p, xrole, xrole ? tile : ptile, part, Mt, T);
 }
 
 }  // namespace
@@ -592,13 +654,15 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   GPTQ_LAUNCH_CHECK();
   {
     dim3 grid((d + 31) / 32, (d + 31) / 32), block(32, 8);
-    prep_gather_kernel<<<grid, block, 0, st>>>(S, diag, perm, d, static_cast<float>(hscale), hscale, lam,
-                                                Z, zlo, U, status);
+    prep_gather_kernel<<<grid, block, 0, st>>>(S, perm, d, static_cast<float>(hscale), Z, U, status);
+    GPTQ_LAUNCH_CHECK();
+    prep_diag_kernel<<<(d + 255) / 256, 256, 0, st>>>(S, diag, perm, d, hscale, lam, Z, zlo, status);
     GPTQ_LAUNCH_CHECK();
   }
-  const size_t smem = sizeof(float) * (3 * NB * LDM + NB + 32 * LDM + 64);
+  const size_t smem = sizeof(float) * (3 * NB * LDM + NB + 32 * LDM + 64 + 32 * LST);
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
+  const int sms = sm_count();
   for (int k = 0; k < d; k += NB) {
     const int b = std::min(NB, d - k);
     PanelArgs pa;
@@ -613,7 +677,11 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     pa.status = status;
     pa.zlo = zlo;
     const int n_pan = (d - k - b + NB - 1) / NB;
-    panel_step_kernel<<<1 + pa.n_acc + n_pan, PT, smem, st>>>(pa);
+    // Split the role tiles over more CTAs while one wave of CTAs still holds
+    // them all (every CTA also factors the diagonal block).
+    const int tiles = pa.n_acc + n_pan;
+    pa.split = (1 + 4 * tiles <= sms) ? 4 : (1 + 2 * tiles <= sms) ? 2 : 1;
+    panel_step_kernel<<<1 + tiles * pa.split, PT, smem, st>>>(pa);
     GPTQ_LAUNCH_CHECK();
     if (k + b < d) {
       TGemmArgs g;

@@ -5,7 +5,7 @@
 //               (A_hi, A_lo, B_hi, B_lo) into a 3-stage ring, 128-byte swizzle
 //   warp 1      MMA issuer: per K slab, 4 steps of K=8, each three
 //               tcgen05.mma kind::tf32 (lo*hi, hi*lo, hi*hi) into TMEM
-//   warps 2-5   epilogue: TMEM -> registers -> C = alpha*acc + beta*C
+//   warps 2-9   epilogue: TMEM -> registers -> C = alpha*acc + beta*C
 // Two 128-column TMEM accumulators let the epilogue of one tile overlap the
 // MMAs of the next.
 #include <algorithm>
@@ -25,7 +25,7 @@ constexpr int UK = 8;   // K of one kind::tf32 MMA
 constexpr int STAGES = 3;
 constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (BN == BM)
 constexpr int STAGE_BYTES = 4 * TILE_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr uint32_t TMEM_COLS = 256;
 
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
-      mbar_init(acce_bar(i), 128);
+      mbar_init(acce_bar(i), 256);
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
@@ -167,54 +167,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait_bounded(drain_bar, 0, fault);
     }
   } else {
+    // Epilogue, 8 warps: warp w reads TMEM lanes 32q..32q+31 (q = w mod 4,
+    // the quarter it may access) and columns 64h..64h+63 of the tile
+    // (h = 0 for warps 2-5, 1 for warps 6-9); each lane owns one row.  The
+    // row's C values are loaded before the accumulator is waited for, so
+    // the read latency overlaps the tile's MMAs.
     const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < s.tiles; t += gridDim.x) {
       int mt, nt;
       tile_coords(a, s, t, mt, nt);
-      if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) break;
-      tc_fence_after();
       const int m = mt * BM + q * 32 + lane;
       const bool row_ok = m < a.M;
       const long long diag = static_cast<long long>(a.row_off) + m - a.col_off;  // n <= diag
       float* crow = a.C + static_cast<int64_t>(m) * a.ldc;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int n0 = nt * BN + c * 32;
-        if (n0 >= a.N) break;
+      float4 cpre[2][8];
+      bool fast[2];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int n0 = nt * BN + h * 64 + cc * 32;
+        fast[cc] = row_ok && (n0 + 32 <= a.N) && (!a.lower || n0 + 31 <= diag) && (a.ldc % 4 == 0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          cpre[cc][i] = (fast[cc] && a.beta != 0.f)
+                            ? *reinterpret_cast<const float4*>(crow + n0 + 4 * i)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int n0 = nt * BN + h * 64 + cc * 32;
+        if (n0 < a.N) {  // warp-uniform
         float v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(acc * BN + c * 32),
+                               static_cast<uint32_t>(acc * BN + h * 64 + cc * 32),
                            v);
-        if (!row_ok) continue;
-        const bool full = (n0 + 32 <= a.N) && (!a.lower || n0 + 31 <= diag);
-        if (a.diag_lo && row_ok && diag >= n0 && diag < n0 + 32 && diag < a.N) {
+        if (row_ok && a.diag_lo && diag >= n0 && diag < n0 + 32 && diag < a.N) {
           // the diagonal element of this row lies in the chunk: two-sum
           const int i = static_cast<int>(diag - n0);
+          float vi = 0.f;  // v[i] without a dynamic index (keeps v in registers)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) vi = (e == i) ? v[e] : vi;
           const float cv = crow[diag];
-          const float t = -v[i];
-          const float sum = cv + t;
+          const float tt = -vi;
+          const float sum = cv + tt;
           const float bb = sum - cv;
-          const float err = (cv - (sum - bb)) + (t - bb);
+          const float err = (cv - (sum - bb)) + (tt - bb);
           a.diag_lo[a.col_off + diag] += err;
         }
-        if (full && (a.ldc % 4 == 0)) {
+        if (row_ok && fast[cc]) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4* p = reinterpret_cast<float4*>(crow + n0 + i);
-            float4 o = make_float4(a.alpha * v[i], a.alpha * v[i + 1], a.alpha * v[i + 2],
-                                   a.alpha * v[i + 3]);
+          for (int i = 0; i < 8; ++i) {
+            float4 o = make_float4(a.alpha * v[4 * i], a.alpha * v[4 * i + 1], a.alpha * v[4 * i + 2],
+                                   a.alpha * v[4 * i + 3]);
             if (a.beta != 0.f) {
-              const float4 cv = *p;
-              o.x = fmaf(a.beta, cv.x, o.x);
-              o.y = fmaf(a.beta, cv.y, o.y);
-              o.z = fmaf(a.beta, cv.z, o.z);
-              o.w = fmaf(a.beta, cv.w, o.w);
+              o.x = fmaf(a.beta, cpre[cc][i].x, o.x);
+              o.y = fmaf(a.beta, cpre[cc][i].y, o.y);
+              o.z = fmaf(a.beta, cpre[cc][i].z, o.z);
+              o.w = fmaf(a.beta, cpre[cc][i].w, o.w);
             }
-            *p = o;
+            *reinterpret_cast<float4*>(crow + n0 + 4 * i) = o;
           }
-        } else {
+        } else if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int n = n0 + i;
@@ -223,6 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (a.beta != 0.f) o = fmaf(a.beta, crow[n], o);
             crow[n] = o;
           }
+        }
         }
       }
       tc_fence_before();
