@@ -46,8 +46,8 @@ WORKLOAD = ("7B attention projection: W bf16 4096x4096 N(0,0.02^2); X fp16 4096x
 # profiles/hessian_syrk_dram_4096x262144tok.md.  It describes the kernel
 # source it was measured on (sha256 prefixes below); once that source
 # changes the figure no longer applies and the bench reports null.
-SYRK_TRAFFIC = {"bytes": 8.90e9, "n_tok": 262144,
-                "sha256": {"hessian_syrk.cu": "96e8cf9c5054e95e", "common.cuh": "fa175be4a21777cc"}}
+SYRK_TRAFFIC = {"bytes": 8.33e9, "n_tok": 262144,
+                "sha256": {"hessian_syrk.cu": "9b0738add5013aeb", "common.cuh": "fa175be4a21777cc"}}
 
 
 def syrk_traffic() -> float | None:
@@ -146,6 +146,22 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest x over all ranks (the job ends when its slowest rank ends)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job rate: every rank processes its own units (weak scaling)."""
+    return world * units_per_rank * steps / seconds
+
+
 # ---------------------------------------------------------------- inputs
 def make_inputs():
     from post_weight_quantization_31_b300 import workloads as wl
@@ -212,11 +228,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     if dist is not None:
         dist.barrier()
     launches = api.launch_count() - n0
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
 
     ph = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
           for i, name in enumerate(("hessian", "prepare", "quantize", "pack"))}
@@ -236,14 +248,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         for _ in range(args.e2e_steps):
             res = api.quantize_layer_from_host(W_host, chunks, cfg, solver=solver)
         torch.cuda.synchronize(dev)
-        e2e_s = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
         h2d = sum(c.numel() * c.element_size() for c in chunks) + W_host.numel() * 2
         d2h = sum(v.numel() * v.element_size() for v in res.values())
-        e2e = {"value": round(world * D * D * args.e2e_steps / e2e_s / 1e6, 3),
+        e2e = {"value": round(job_throughput(D * D, args.e2e_steps, world, e2e_s) / 1e6, 3),
                "unit": "Mweights/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "steps": args.e2e_steps}
 
@@ -266,7 +274,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     ms_step = elapsed_ms / args.steps
     line = {
         "metric": METRIC,
-        "value": round(world * D * D * args.steps / (elapsed_ms * 1e-3) / 1e6, 3),
+        "value": round(job_throughput(D * D, args.steps, world, elapsed_ms * 1e-3) / 1e6, 3),
         "unit": "Mweights/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
