@@ -167,9 +167,8 @@ GPTQ_API gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int
  * latency-critical path where cudaMalloc / cudaFree would synchronize the
  * device.  It computes exactly what gptq_prepare_hinv computes, with the
  * same arguments except ws / ws_bytes, and allocates nothing: the scratch
- * space is a fixed array of about 6.3 MB that the library keeps in device
- * memory on every GPU it is loaded on, until the process exits.  All its
- * work runs on `stream` (gptq_prepare_hinv also uses a helper stream).
+ * space is a fixed array of about 5.3 MB that the library keeps in device
+ * memory on every GPU it is loaded on, until the process exits.
  *   d_col   at most GPTQ_NOALLOC_MAX_D_COL (1024); larger values return
  *           GPTQ_ERR_WORKSPACE with no side effect.  Other argument errors
  *           and status codes are those of gptq_prepare_hinv.

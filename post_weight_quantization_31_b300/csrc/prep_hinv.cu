@@ -30,7 +30,6 @@
 //                  (-P X_k), the rest the Schur update (-P P^T).
 // Cost ~ 2 d^3 / 3 flop, all of it in the tensor-core GEMMs except O(d nb^2).
 #include <algorithm>
-#include <mutex>
 
 #include "common.cuh"
 #include "tgemm.cuh"
@@ -601,7 +600,7 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct PrepLayout {
-  size_t status, lam, keys, zlo, Z, Bhi[2], Blo[2], total;
+  size_t status, lam, keys, zlo, Z, Bhi, Blo, total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -619,45 +618,19 @@ static PrepLayout prep_layout(int64_t d) {
   off = align256(off + sizeof(float) * d);
   L.Z = off;
   off = align256(off + sizeof(float) * d * d);
-  for (int i = 0; i < 2; ++i) {  // the panel operand, by step parity
-    L.Bhi[i] = off;
-    off = align256(off + sizeof(float) * d * NB);
-    L.Blo[i] = off;
-    off = align256(off + sizeof(float) * d * NB);
-  }
+  L.Bhi = off;
+  off = align256(off + sizeof(float) * d * NB);
+  L.Blo = off;
+  off = align256(off + sizeof(float) * d * NB);
   L.total = off;
   return L;
 }
 
 size_t prep_workspace_bytes(int64_t d) { return prep_layout(d).total; }
 
-// A helper stream and four events per device for the look-ahead schedule,
-// created on first use and kept for the life of the process.
-struct LookaheadRes {
-  cudaStream_t helper = nullptr;
-  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
-};
-
-static LookaheadRes* lookahead_res() {
-  static std::mutex mu;
-  static LookaheadRes res[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  LookaheadRes& r = res[dev];
-  if (!r.helper) {
-    cudaStream_t h = nullptr;
-    if (cudaStreamCreateWithFlags(&h, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    for (int i = 0; i < 4; ++i)
-      if (cudaEventCreateWithFlags(&r.ev[i], cudaEventDisableTiming) != cudaSuccess) return nullptr;
-    r.helper = h;
-  }
-  return &r;
-}
-
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, int64_t n_seen,
                              float damp, bool desc_act, float* U, int32_t* perm, void* ws,
-                             cudaStream_t st, int* status_host, bool lookahead) {
+                             cudaStream_t st, int* status_host) {
   const int d = static_cast<int>(d64);
   const PrepLayout L = prep_layout(d64);
   char* base = static_cast<char*>(ws);
@@ -666,20 +639,9 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   auto* keys = reinterpret_cast<unsigned long long*>(base + L.keys);
   float* Z = reinterpret_cast<float*>(base + L.Z);
   float* zlo = reinterpret_cast<float*>(base + L.zlo);
-  float* Bhi[2] = {reinterpret_cast<float*>(base + L.Bhi[0]), reinterpret_cast<float*>(base + L.Bhi[1])};
-  float* Blo[2] = {reinterpret_cast<float*>(base + L.Blo[0]), reinterpret_cast<float*>(base + L.Blo[1])};
+  float* Bhi = reinterpret_cast<float*>(base + L.Bhi);
+  float* Blo = reinterpret_cast<float*>(base + L.Blo);
   const double hscale = 2.0 / static_cast<double>(n_seen);
-  LookaheadRes* la = nullptr;
-  // The helper stream and events are shared by every call on the device:
-  // one host thread at a time enqueues a look-ahead schedule (each call's
-  // event waits then refer to its own records).
-  static std::mutex enqueue_mu;
-  std::unique_lock<std::mutex> enqueue_lock(enqueue_mu, std::defer_lock);
-  if (lookahead && d > 2 * NB) {
-    la = lookahead_res();
-    if (!la) return GPTQ_ERR_CUDA;
-    enqueue_lock.lock();
-  }
 
   GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
   prep_stats_kernel<<<1, 1024, 0, st>>>(S, diag, d, hscale, damp, keys, lam, status);
@@ -701,117 +663,44 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)));
   const int sms = sm_count();
-
-  // Update after step k: Z[k+b:, :] (lower) -= P B^T with this step's B.
-  auto update_args = [&](int k, int b, int mode) {
-    TGemmArgs g;
-    g.M = d - k - b;
-    g.N = d;
-    g.K = NB;
-    g.alpha = -1.f;
-    g.beta = 1.f;
-    g.C = Z + static_cast<int64_t>(k + b) * d;
-    g.ldc = d;
-    g.lower = 1;
-    g.row_off = k + b;
-    g.col_off = 0;
-    g.diag_lo = zlo;
-    g.mode = mode;
-    g.skip_nt = (k + b) / NB;  // the tile column of the next diagonal block
-    return g;
-  };
-  auto update = [&](int k, const TGemmArgs& g, cudaStream_t s) -> gptq_status_t {
-    const int par = (k / NB) & 1;
-    const int row0 = g.row_off;
-    return launch_tgemm_3xtf32(Bhi[par] + static_cast<int64_t>(row0) * NB,
-                               Blo[par] + static_cast<int64_t>(row0) * NB, NB, Bhi[par], Blo[par], NB, g,
-                               s);
-  };
-  auto role_tiles = [&](int k) {
-    const int b = std::min(NB, d - k);
-    return (k + NB - 1) / NB + (d - k - b + NB - 1) / NB;
-  };
-  // Most CTAs per role tile that one wave of the GPU holds (each CTA also
-  // factors the diagonal block).
-  auto split_alone = [&](int k) {
-    const int t = role_tiles(k);
-    return (1 + 4 * t <= sms) ? 4 : (1 + 2 * t <= sms) ? 2 : 1;
-  };
-  // With look-ahead, panel(k) shares the GPU with the previous step's bulk
-  // update of `bulk_tiles` tiles: pick the split that balances the two.
-  // Cost model in microseconds (measured orders of magnitude): factorization
-  // 26, role products 16 / split, one update tile 8 per CTA.
-  auto split_shared = [&](int k, int bulk_tiles) {
-    const int t = role_tiles(k);
-    double best = 1e30;
-    int split = 1;
-    for (int sp = 1; sp <= 4; sp *= 2) {
-      const int ctas = 1 + t * sp;
-      if (ctas >= sms) break;
-      const double tt = std::max(26.0 + 16.0 / sp, bulk_tiles * 8.0 / (sms - ctas));
-      if (tt < best - 1e-9) {
-        best = tt;
-        split = sp;
-      }
-    }
-    return split;
-  };
-
-  // Schedule.  Without look-ahead: panel(k), then the whole update, on the
-  // caller's stream.  With look-ahead, after panel(k) only the part of the
-  // update that panel(k+1) reads (mode 1: the next diagonal block's tile row
-  // and tile column) runs on the caller's stream; the rest (mode 2) runs on
-  // the helper stream, on the SMs panel(k+1) leaves free, while panel(k+1)
-  // runs.  The next mode-1 update waits for it (both write the same rows),
-  // and the operand B alternates between two buffers so that panel(k+1) does
-  // not overwrite what the helper reads.
-  int split = split_alone(0);
   for (int k = 0; k < d; k += NB) {
     const int b = std::min(NB, d - k);
-    const int par = (k / NB) & 1;
     PanelArgs pa;
     pa.Z = Z;
     pa.n = d;
     pa.k = k;
     pa.b = b;
     pa.n_acc = (k + NB - 1) / NB;
-    pa.Bhi = Bhi[par];
-    pa.Blo = Blo[par];
+    pa.Bhi = Bhi;
+    pa.Blo = Blo;
     pa.U = U;
     pa.status = status;
     pa.zlo = zlo;
-    pa.split = split;
-    panel_step_kernel<<<1 + role_tiles(k) * pa.split, PT, smem, st>>>(pa);
+    const int n_pan = (d - k - b + NB - 1) / NB;
+    // Split the role tiles over more CTAs while one wave of CTAs still holds
+    // them all (every CTA also factors the diagonal block).
+    const int tiles = pa.n_acc + n_pan;
+    pa.split = (1 + 4 * tiles <= sms) ? 4 : (1 + 2 * tiles <= sms) ? 2 : 1;
+    panel_step_kernel<<<1 + tiles * pa.split, PT, smem, st>>>(pa);
     GPTQ_LAUNCH_CHECK();
-    if (k + b >= d) break;
-    if (!la) {
-      const gptq_status_t s = update(k, update_args(k, b, 0), st);
+    if (k + b < d) {
+      TGemmArgs g;
+      g.M = d - k - b;
+      g.N = d;
+      g.K = NB;
+      g.alpha = -1.f;
+      g.beta = 1.f;
+      g.C = Z + static_cast<int64_t>(k + b) * d;
+      g.ldc = d;
+      g.lower = 1;
+      g.row_off = k + b;
+      g.col_off = 0;
+      g.diag_lo = zlo;
+      const gptq_status_t s = launch_tgemm_3xtf32(Bhi + static_cast<int64_t>(k + b) * NB,
+                                                  Blo + static_cast<int64_t>(k + b) * NB, NB, Bhi, Blo,
+                                                  NB, g, st);
       if (s != GPTQ_OK) return s;
-      split = split_alone(k + NB);
-      continue;
     }
-    // Before this step's mode-1 update, the previous step's bulk update
-    // (same rows) must be done.
-    if (k > 0) GPTQ_CUDA_TRY(cudaStreamWaitEvent(st, la->ev[2 + ((k / NB - 1) & 1)], 0));
-    gptq_status_t s = update(k, update_args(k, b, 1), st);
-    if (s != GPTQ_OK) return s;
-    split = split_alone(k + NB);
-    if (k + b + NB < d) {  // rows beyond the next diagonal block remain
-      TGemmArgs g = update_args(k, b, 2);
-      split = split_shared(k + NB, tgemm_tile_count(g));
-      g.max_ctas = std::max(1, sms - (1 + role_tiles(k + NB) * split));
-      cudaEvent_t ea = la->ev[par], eb = la->ev[2 + par];
-      GPTQ_CUDA_TRY(cudaEventRecord(ea, st));
-      GPTQ_CUDA_TRY(cudaStreamWaitEvent(la->helper, ea, 0));
-      s = update(k, g, la->helper);
-      if (s != GPTQ_OK) return s;
-      GPTQ_CUDA_TRY(cudaEventRecord(eb, la->helper));
-    }
-  }
-  // The last bulk update must be complete before the status is read.
-  if (la && d > 2 * NB) {
-    const int k_last_bulk = ((d - 1) / NB - 2) * NB;  // last step that launched a bulk update
-    if (k_last_bulk >= 0) GPTQ_CUDA_TRY(cudaStreamWaitEvent(st, la->ev[2 + ((k_last_bulk / NB) & 1)], 0));
   }
   GPTQ_CUDA_TRY(cudaMemcpyAsync(status_host, status, sizeof(int), cudaMemcpyDeviceToHost, st));
   return GPTQ_OK;

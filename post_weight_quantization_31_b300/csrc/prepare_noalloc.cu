@@ -14,9 +14,6 @@
 namespace gptq {
 
 size_t prep_workspace_bytes(int64_t d);
-gptq_status_t prepare_hinv_impl(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
-                                const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
-                                size_t ws_bytes, gptq_stream_t stream, bool lookahead);
 
 namespace {
 
@@ -24,10 +21,10 @@ constexpr int64_t kMaxDCol = GPTQ_NOALLOC_MAX_D_COL;
 constexpr size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Room for the prepare workspace at d_col = kMaxDCol: status and damping
 // words, the 64-bit sort keys, the low parts of the work matrix's diagonal,
-// the d x d work matrix and two pairs of d x 128 panel operands.  Each call
+// the d x d work matrix and the two d x 128 panel operands.  Each call
 // checks it against prep_workspace_bytes().
 constexpr size_t kScratchBytes = 256 + 256 + round256(8 * kMaxDCol) + round256(4 * kMaxDCol) +
-                                 round256(4 * kMaxDCol * kMaxDCol) + 4 * round256(4 * kMaxDCol * 128);
+                                 round256(4 * kMaxDCol * kMaxDCol) + 2 * round256(4 * kMaxDCol * 128);
 
 static __device__ __align__(256) unsigned char g_prep_scratch[kScratchBytes];
 
@@ -59,7 +56,5 @@ extern "C" GPTQ_API gptq_status_t gptq_prepare_hinv_noalloc(const float* S, cons
   if (d_col > 0 && gptq::prep_workspace_bytes(d_col) > gptq::kScratchBytes) return GPTQ_ERR_WORKSPACE;
   void* ws = gptq::scratch_address();
   if (!ws) return GPTQ_ERR_CUDA;
-  // Everything on the caller's stream: no helper stream or events are created.
-  return gptq::prepare_hinv_impl(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream,
-                                 false);
+  return gptq_prepare_hinv(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream);
 }

@@ -33,46 +33,22 @@ struct TGemmSched {
   int m_tiles, n_tiles, k_blocks, tiles;
 };
 
-// Tiles of tile row mt allowed by the lower-triangle limit.
-__host__ __device__ __forceinline__ int lim_tiles(const TGemmArgs& a, int n_tiles, int mt) {
-  if (!a.lower) return n_tiles;
+__device__ __forceinline__ int n_tiles_for_row(const TGemmArgs& a, const TGemmSched& s, int mt) {
+  if (!a.lower) return s.n_tiles;
   const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM - 1 -
                         a.col_off;
   if (lim < 0) return 0;
-  return static_cast<int>(lim / BN + 1 < n_tiles ? lim / BN + 1 : n_tiles);
-}
-
-// Selected tiles of tile row mt (see TGemmArgs::mode); with idx, the tile
-// column of the idx-th of them.
-__host__ __device__ __forceinline__ int row_tiles(const TGemmArgs& a, int n_tiles, int mt, int idx,
-                                                  int* nt) {
-  const int c = lim_tiles(a, n_tiles, mt);
-  const bool has_skip = a.skip_nt < c;
-  if (a.mode == 1) {
-    if (mt == 0) {
-      if (nt) *nt = idx;
-      return c;
-    }
-    if (nt) *nt = a.skip_nt;
-    return has_skip ? 1 : 0;
-  }
-  if (a.mode == 2) {
-    if (mt == 0) return 0;
-    if (nt) *nt = (has_skip && idx >= a.skip_nt) ? idx + 1 : idx;
-    return has_skip ? c - 1 : c;
-  }
-  if (nt) *nt = idx;
-  return c;
+  return static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
 }
 
 __device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
                                             int& nt) {
   for (mt = 0; mt < s.m_tiles; ++mt) {
-    const int c = row_tiles(a, s.n_tiles, mt, 0, nullptr);
+    const int c = n_tiles_for_row(a, s, mt);
     if (t < c) break;
     t -= c;
   }
-  row_tiles(a, s.n_tiles, mt, t, &nt);
+  nt = t;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -313,17 +289,21 @@ TGemmSched make_sched(const TGemmArgs& a) {
   s.n_tiles = (a.N + BN - 1) / BN;
   s.k_blocks = (a.K + BK - 1) / BK;
   s.tiles = 0;
-  for (int mt = 0; mt < s.m_tiles; ++mt) s.tiles += row_tiles(a, s.n_tiles, mt, 0, nullptr);
+  for (int mt = 0; mt < s.m_tiles; ++mt) {
+    int c = s.n_tiles;
+    if (a.lower) {
+      const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM -
+                            1 - a.col_off;
+      c = lim < 0 ? 0 : static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
+    }
+    s.tiles += c;
+  }
   return s;
 }
 
 }  // namespace
 
 int tgemm_tile_count(const TGemmArgs& args) { return make_sched(args).tiles; }
-
-int tiles_of_row(const TGemmArgs& a, int n_tiles, int mt, int idx, int* nt) {
-  return row_tiles(a, n_tiles, mt, idx, nt);
-}
 
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
                                   const float* B_lo, int64_t ldb, const TGemmArgs& args,
@@ -343,7 +323,7 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
                                        SMEM_BYTES));
     attr_dev = dev;
   }
-  const int grid = std::min(args.max_ctas > 0 ? args.max_ctas : sm_count(), s.tiles);
+  const int grid = std::min(sm_count(), s.tiles);
   tgemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m_ahi, m_alo, m_bhi, m_blo, args, s,
                                                       fault_word_ptr());
   GPTQ_LAUNCH_CHECK();
@@ -372,35 +352,4 @@ extern "C" GPTQ_API int gptq_internal_tgemm(const float* A_hi, const float* A_lo
   g.col_off = col_off;
   return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g,
                                    reinterpret_cast<cudaStream_t>(stream));
-}
-
-// Test hook: the (tile row, tile column) list a launch with these arguments
-// processes, in processing order (at most `cap` entries written); returns the
-// number of tiles.
-extern "C" GPTQ_API int gptq_internal_tgemm_tiles(int M, int N, int lower, int row_off, int col_off,
-                                                  int mode, int skip_nt, int32_t* mt_out, int32_t* nt_out,
-                                                  int cap) {
-  gptq::TGemmArgs g;
-  g.M = M;
-  g.N = N;
-  g.K = 128;
-  g.lower = lower;
-  g.row_off = row_off;
-  g.col_off = col_off;
-  g.mode = mode;
-  g.skip_nt = skip_nt;
-  const int m_tiles = (M + 127) / 128, n_tiles = (N + 127) / 128;
-  int count = 0;
-  for (int mt = 0; mt < m_tiles; ++mt) {
-    const int c = gptq::tiles_of_row(g, n_tiles, mt, 0, nullptr);
-    for (int i = 0; i < c; ++i, ++count) {
-      int nt = 0;
-      gptq::tiles_of_row(g, n_tiles, mt, i, &nt);
-      if (count < cap) {
-        mt_out[count] = mt;
-        nt_out[count] = nt;
-      }
-    }
-  }
-  return count;
 }

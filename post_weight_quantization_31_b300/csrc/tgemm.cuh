@@ -31,14 +31,6 @@ struct TGemmArgs {
   // update (Knuth two-sum) is added to diag_lo[col_off + n], so that
   // C + diag_lo carries the running diagonal to about twice fp32 precision.
   float* diag_lo = nullptr;
-  // Tile selection (with `lower`): 0 all tiles; 1 only the tiles of the
-  // first tile row and of tile column skip_nt; 2 all the others.  Modes 1
-  // and 2 split one update into the part the next factorization step reads
-  // and the rest.
-  int mode = 0;
-  int skip_nt = 0;
-  // Upper bound on CTAs (0: one per SM, persistent over tiles).
-  int max_ctas = 0;
 };
 
 // hi: x rounded to a TF32 value (10 explicit mantissa bits, ties away);
@@ -61,9 +53,5 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
 
 // Number of 128 x 128 output tiles the launch above would process.
 int tgemm_tile_count(const TGemmArgs& args);
-
-// Selected tiles of tile row mt (TGemmArgs::mode); with idx, the tile
-// column of the idx-th of them in *nt.
-int tiles_of_row(const TGemmArgs& a, int n_tiles, int mt, int idx, int* nt);
 
 }  // namespace gptq

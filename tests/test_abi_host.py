@@ -160,34 +160,3 @@ def test_syrk_schedule_covers_all_tiles(lib, d):
 def test_syrk_schedule_small_token_count(lib):
     s = schedule(lib, 512, 2048, 148)
     assert s["ks"] <= 2048 // 64 // 8
-
-
-@pytest.mark.parametrize("d,k", [(4096, 0), (4096, 1920), (2080, 1792), (1024, 640), (11008, 5120)])
-def test_lookahead_updates_partition_the_trailing_update(lib, d, k):
-    """The two halves of one step's update (the tiles the next factorization
-    step reads, then the rest) are disjoint and together give exactly the
-    tiles of the whole update."""
-    f = lib.gptq_internal_tgemm_tiles
-    f.restype = ctypes.c_int
-    i32p = ctypes.POINTER(ctypes.c_int32)
-    f.argtypes = [ctypes.c_int] * 7 + [i32p, i32p, ctypes.c_int]
-    b = 128
-    M, N, row_off, skip = d - k - b, d, k + b, (k + b) // 128
-
-    def tiles(mode):
-        cap = 200000
-        mt = (ctypes.c_int32 * cap)()
-        nt = (ctypes.c_int32 * cap)()
-        n = f(M, N, 1, row_off, 0, mode, skip, mt, nt, cap)
-        return [(mt[i], nt[i]) for i in range(n)]
-
-    full, near, rest = tiles(0), tiles(1), tiles(2)
-    assert len(set(full)) == len(full)
-    assert set(near) | set(rest) == set(full)
-    assert not set(near) & set(rest)
-    # the next diagonal block's tile row and tile column are in the first half
-    assert all(mt == 0 or nt == skip for mt, nt in near)
-    assert all(mt > 0 and nt != skip for mt, nt in rest)
-    # lower triangle: a tile is present iff its first column <= its last row
-    for mt, nt in full:
-        assert nt * 128 <= row_off + mt * 128 + 127
