@@ -546,6 +546,10 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
   const bool xrole = role >= 1 && tile < p.n_acc;
   const int ptile = tile - p.n_acc;  // P role: panel tile index
   const int prow = NB / p.split;     // rows of the P operand this CTA needs
+  // Launched with programmatic dependent launch: Z and B come from the
+  // previous kernels.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // Role operand tile, fetched while the diagonal block is factored.
   if (role >= 1) {
@@ -681,7 +685,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     // them all (every CTA also factors the diagonal block).
     const int tiles = pa.n_acc + n_pan;
     pa.split = (1 + 4 * tiles <= sms) ? 4 : (1 + 2 * tiles <= sms) ? 2 : 1;
-    panel_step_kernel<<<1 + tiles * pa.split, PT, smem, st>>>(pa);
+    GPTQ_CUDA_TRY(launch_pdl(panel_step_kernel, dim3(1 + tiles * pa.split), dim3(PT), smem, st, pa));
     GPTQ_LAUNCH_CHECK();
     if (k + b < d) {
       TGemmArgs g;

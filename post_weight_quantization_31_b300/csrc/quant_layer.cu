@@ -191,6 +191,10 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
   __syncthreads();
   for (int jj = tid; jj < CB; jj += CL_THREADS)
     inv_d[jj] = jj < nc ? 1.f / Us[jj * UROW + (jj / CPL) * USEG + (jj % CPL)] : 0.f;
+  // U is read-only here: the loads above may overlap the previous kernel
+  // (programmatic dependent launch); W, Err, codes and scales may not.
+  griddep_wait();
+  griddep_launch_dependents();
 
   float w[CPL];
   const bool row_ok = r < a.d_row;
@@ -424,7 +428,8 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
       ca.Err_hi = Err_hi;
       ca.Err_lo = Err_lo;
       ca.err_col0 = i1 - sb0;
-      column_block_kernel<<<(d_row + CL_ROWS - 1) / CL_ROWS, CL_THREADS, kColumnSmem, st>>>(ca);
+      GPTQ_CUDA_TRY(launch_pdl(column_block_kernel, dim3((d_row + CL_ROWS - 1) / CL_ROWS),
+                               dim3(CL_THREADS), kColumnSmem, st, ca));
       GPTQ_LAUNCH_CHECK();
       const int i2 = i1 + nc;
       if (i2 < sb1) {

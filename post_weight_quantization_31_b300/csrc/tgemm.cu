@@ -93,6 +93,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above is independent of the previous kernel (launched with
+  // programmatic dependent launch); A, B and C are not.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -324,8 +328,8 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
     attr_dev = dev;
   }
   const int grid = std::min(sm_count(), s.tiles);
-  tgemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(m_ahi, m_alo, m_bhi, m_blo, args, s,
-                                                      fault_word_ptr());
+  GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, m_ahi, m_alo,
+                           m_bhi, m_blo, args, s, fault_word_ptr()));
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
