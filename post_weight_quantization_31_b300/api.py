@@ -238,12 +238,12 @@ class LayerSolver:
         self.qweight = torch.empty((d_col * cfg.bits // 32, d_row), dtype=torch.int32, device=dev)
         self.qzeros = torch.empty((G, d_row * cfg.bits // 32), dtype=torch.int32, device=dev)
 
-    def staging(self, tokens: int) -> list:
-        """Two device buffers [d_col, tokens] fp16 for chunked host input."""
+    def staging(self, tokens: int, count: int = 2) -> list:
+        """`count` device buffers [d_col, tokens] fp16 for chunked host input."""
         cur = getattr(self, "_stage", None)
-        if cur is None or cur[0].shape[1] < tokens:
+        if cur is None or cur[0].shape[1] < tokens or len(cur) != count:
             self._stage = [torch.empty((self.d_col, tokens), dtype=torch.float16,
-                                       device=self.device) for _ in range(2)]
+                                       device=self.device) for _ in range(count)]
         return self._stage
 
     def w_buffer(self, dtype) -> torch.Tensor:
@@ -288,43 +288,52 @@ class LayerSolver:
 
 
 def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
-                             solver: LayerSolver | None = None) -> dict:
+                             solver: LayerSolver | None = None, copy_streams: int = 2) -> dict:
     """End to end from host memory.
 
     X_chunks: sequence of host fp16 tensors [d_col, t_i] (contiguous; pinned
     for asynchronous copies), e.g. one per batch of calibration sequences.
-    Chunks are copied to the device on a side stream into two alternating
-    staging buffers, overlapped with the Hessian accumulation of the
-    previous chunk; then the layer is solved and the packed result
-    (qweight, qzeros, scales, g_idx) is returned in host memory.
+    Chunks are copied to the device on `copy_streams` side streams (chunk i
+    on stream i mod copy_streams, so that several copy engines can run at
+    once) into rotating staging buffers, overlapped with the Hessian
+    accumulation of the chunks already copied; then the layer is solved and
+    the packed result (qweight, qzeros, scales, g_idx) is returned in host
+    memory.
     """
     d_row, d_col = W_host.shape
     solver = solver or LayerSolver(d_row, d_col, cfg)
     solver.reset()
     dev = solver.device
     compute = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
+    n_copy = max(1, int(copy_streams))
+    copies = getattr(solver, "_copy_streams", None)
+    if copies is None or len(copies) != n_copy:
+        copies = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+        solver._copy_streams = copies
     cap = max(int(c.shape[1]) for c in X_chunks)
     cap = (cap + 7) // 8 * 8
-    stage = solver.staging(cap)
+    stage = solver.staging(cap, count=n_copy + 1)
     ready = [torch.cuda.Event() for _ in stage]
     free = [torch.cuda.Event() for _ in stage]
+    used = [False] * len(stage)
     W_dev = solver.w_buffer(W_host.dtype)
-    with torch.cuda.stream(copy):
+    with torch.cuda.stream(copies[0]):
         W_dev.copy_(W_host, non_blocking=True)
     w_ready = torch.cuda.Event()
-    w_ready.record(copy)
+    w_ready.record(copies[0])
     for ci, chunk in enumerate(X_chunks):
         if chunk.shape[0] != d_col or chunk.dtype != torch.float16:
             raise ValueError("each X chunk must be fp16 [d_col, t]")
         b = ci % len(stage)
+        cs = copies[ci % n_copy]
         t = int(chunk.shape[1])
         buf = stage[b][:, :t]
-        with torch.cuda.stream(copy):
-            if ci >= len(stage):
-                copy.wait_event(free[b])
+        with torch.cuda.stream(cs):
+            if used[b]:
+                cs.wait_event(free[b])
             buf.copy_(chunk, non_blocking=True)
-            ready[b].record(copy)
+            ready[b].record(cs)
+        used[b] = True
         compute.wait_event(ready[b])
         solver.accumulate(buf)
         free[b].record(compute)

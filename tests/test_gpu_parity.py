@@ -182,3 +182,28 @@ def test_pack_unpack_bit_exact(bits, d_row, d_col, gs):
     c2, z2 = api.unpack(qw, qz, d_row, d_col, bits, gs)
     assert np.array_equal(c2.cpu().numpy(), codes)
     assert np.array_equal(z2.cpu().numpy(), zeros)
+
+
+@pytest.mark.parametrize("copy_streams", [1, 2])
+def test_host_buffer_path_matches_oracle(copy_streams):
+    """The end-to-end call (pinned host chunks -> side-stream copies ->
+    accumulate -> solve -> packed host result) against the oracle."""
+    import torch
+    from post_weight_quantization_31_b300 import api
+    inp = wl.tiny_layer()
+    d_row, d_col = inp.W.shape
+    chunks = [torch.from_numpy(np.ascontiguousarray(inp.X[:, a:a + 300])).pin_memory()
+              for a in range(0, inp.X.shape[1], 300)]                    # ragged last chunk
+    W_host = torch.from_numpy(inp.W).pin_memory()
+    out = api.quantize_layer_from_host(W_host, chunks, inp.cfg, copy_streams=copy_streams)
+    bits = inp.cfg.bits
+    codes = O.unpack_qweight(out["qweight"].numpy(), bits, d_col)
+    S64 = O.hessian_sum(inp.X)
+    ref = O.quantize_layer(inp.W, S64, inp.X.shape[1], inp.cfg)
+    assert (codes == ref.codes).mean() >= P.CODE_MATCH
+    assert np.abs(codes - ref.codes).max() <= 1
+    assert np.array_equal(out["g_idx"].numpy(), ref.g_idx)
+    srel = np.abs(out["scales"].numpy().astype(np.float64) - ref.scales) / ref.scales
+    assert srel.max() <= P.SCALE_RTOL
+    zeros = O.unpack_qzeros(out["qzeros"].numpy(), bits, d_row)
+    assert (zeros == ref.zeros).mean() >= P.CODE_MATCH
