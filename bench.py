@@ -15,6 +15,11 @@ Prints one JSON line (rank 0).  Metric: weights quantized per second
 layer (weak scaling, no collective on the data path); the time is the max
 over ranks.
 
+The line also carries "dequant": gptq_dequantize of the solved layer's
+packed output to fp16, timed per launch with an L2 flush (the consumer of the
+packed format).  --dequant-only ROWSxCOLS times that kernel alone on a random
+packed 4-bit g128 layer of the given shape (bf16 output).
+
 --impl reference times the CPU oracle (the same algorithm in NumPy fp64) on
 a bounded sample of the same workload and extrapolates to the full layer.
 """
@@ -46,8 +51,8 @@ WORKLOAD = ("7B attention projection: W bf16 4096x4096 N(0,0.02^2); X fp16 4096x
 # profiles/hessian_syrk_dram_4096x262144tok.md.  It describes the kernel
 # source it was measured on (sha256 prefixes below); once that source
 # changes the figure no longer applies and the bench reports null.
-SYRK_TRAFFIC = {"bytes": 8.33e9, "n_tok": 262144,
-                "sha256": {"hessian_syrk.cu": "9b0738add5013aeb", "common.cuh": "fa175be4a21777cc"}}
+SYRK_TRAFFIC = {"bytes": 8.466e9, "n_tok": 262144,
+                "sha256": {"hessian_syrk.cu": "9b0738add5013aeb", "common.cuh": "0ee3a6d05cd5b784"}}
 
 
 def syrk_traffic() -> float | None:
@@ -289,11 +294,80 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         "clocks": clk.summary(),
         "e2e": e2e,
     }
+    if args.dequant_reps > 0:
+        line["dequant"] = measure_dequant(solver, cfg, stream, peaks, args.dequant_reps)
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, quick=args.quick_cpu)
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+def measure_dequant(solver, cfg, stream, peaks: dict, reps: int) -> dict:
+    """gptq_dequantize of the solved layer's packed output to fp16."""
+    import torch
+    return time_dequant(solver.qweight, solver.qzeros, solver.out["scales"], solver.out["g_idx"],
+                        D, D, cfg.bits, cfg.group_size, torch.float16, stream, peaks, reps)
+
+
+def time_dequant(qweight, qzeros, scales, g_idx, d_row, d_col, bits, group_size, dtype, stream,
+                 peaks: dict, reps: int) -> dict:
+    """Dequantization timed per launch with CUDA events on `stream`.  L2
+    (126 MB) is flushed before each launch by reading a 256 MB buffer (a read
+    leaves clean lines, so no write-back of earlier data lands inside the
+    timed launch).  Algorithmic bytes: the packed words, zeros, scales and
+    g_idx read once, the dense weights written once."""
+    import torch
+    from post_weight_quantization_31_b300 import api
+    dev = qweight.device
+    flush = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    out = torch.empty((d_row, d_col), dtype=dtype, device=dev)
+    args = (qweight, qzeros, scales, g_idx, d_row, d_col, bits, group_size)
+    for _ in range(2):
+        api.dequantize(*args, dtype=dtype, out=out)
+    ms = []
+    for _ in range(reps):
+        flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        api.dequantize(*args, dtype=dtype, out=out)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    nbytes = sum(t.numel() * t.element_size() for t in (qweight, qzeros, scales, g_idx, out))
+    t = statistics.median(ms)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", 6400.0))
+    tname = {torch.float16: "fp16", torch.bfloat16: "bf16", torch.float32: "fp32"}[dtype]
+    return {"kernel": f"dequant_kernel ({d_row}x{d_col} {bits}-bit g{group_size} -> {tname})",
+            "median_us": round(t * 1e3, 2), "bytes": int(nbytes), "reps": reps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_note": f"{peaks['source']} copy bandwidth"}}
+
+
+def run_dequant_only(args) -> dict:
+    """--dequant-only ROWSxCOLS: one packed 4-bit g128 layer (random codes,
+    zeros and scales; packed by the library), dequantized to bf16."""
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib
+    build_lib.build()
+    d_row, d_col = (int(v) for v in args.dequant_only.lower().split("x"))
+    bits, gs = 4, 128
+    G = d_col // gs
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    codes = torch.randint(0, 1 << bits, (d_row, d_col), dtype=torch.uint8, device="cuda", generator=gen)
+    zeros = torch.randint(0, 1 << bits, (G, d_row), dtype=torch.uint8, device="cuda", generator=gen)
+    qweight, qzeros = api.pack(codes, zeros, bits, gs)
+    del codes
+    scales = torch.rand((G, d_row), device="cuda", generator=gen) * 0.02 + 1e-3
+    g_idx = (torch.arange(d_col, device="cuda", dtype=torch.int32) // gs).contiguous()
+    res = time_dequant(qweight, qzeros, scales, g_idx, d_row, d_col, bits, gs, torch.bfloat16,
+                       torch.cuda.current_stream(), measured_peaks(), max(1, args.dequant_reps))
+    return {"metric": "dequantized weights GB/s (algorithmic bytes)", "value": res["roofline"]["achieved"],
+            "unit": "GB/s", "n_gpus": 1, "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": f"packed {d_row}x{d_col} 4-bit g128 layer -> bf16, no act-order",
+                       "l2": "flushed by a 256 MB read before each launch"},
+            "dequant": res}
 
 
 # ---------------------------------------------------------------- oracle arm
@@ -391,6 +465,10 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--dequant-reps", type=int, default=20,
+                    help="timed launches of the packed-layer dequantization (0: skip)")
+    ap.add_argument("--dequant-only", default=None, metavar="ROWSxCOLS",
+                    help="time only the dequantization of a packed layer of this shape")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     ap.add_argument("--syrk-traffic", type=float, default=None,
                     help="DRAM bytes per Hessian launch from an ncu capture")
@@ -403,7 +481,9 @@ def main() -> None:
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.dequant_only:
+        line = run_dequant_only(args)
+    elif args.impl == "reference":
         line = run_reference(args, rank)
     else:
         if args.warmup < 3:

@@ -235,6 +235,32 @@ GPTQ_API gptq_status_t gptq_unpack(const int32_t* qweight, const int32_t* qzeros
                           int64_t d_col, int32_t bits, int32_t group_size, uint8_t* codes,
                           uint8_t* zeros, gptq_stream_t stream);
 
+/*
+ * The packed layer back to dense weights, in the ORIGINAL column order:
+ *   W_out[r][c] = scales[g][r] * (code[r][c] - zero[g][r]),  g = g_idx[c],
+ * formed in fp32 and rounded to nearest in out_dtype (GPTQ_W_FP32 / _BF16 /
+ * _FP16).  With desc_act the columns of a group are scattered and g_idx
+ * re-orders them, as the guide's §5.2 says happens when such a model is
+ * loaded ([G] §5.2); this is the consumer that checks the packed format
+ * end to end.
+ *   qweight, qzeros  layouts of gptq_pack; qweight 16-byte aligned.
+ *   scales           fp32 [G, d_row].
+ *   g_idx            int32 [d_col], 16-byte aligned, values in [0, G)
+ *                    (others are clamped into range, so the result is then
+ *                    undefined but no memory outside the arrays is read).
+ *   W_out            [d_row, d_col] of out_dtype, 16-byte aligned.
+ *   d_row % 32 == 0, d_col % 32 == 0, group_size as in gptq_pack.
+ *   All pointers are device memory owned by the caller.  Asynchronous;
+ *   GPTQ_ERR_INVALID_ARG for bad sizes, types or alignment.  The kernel's
+ *   internal waits are bounded: if one runs out, the library's fault flag
+ *   is set and the next gptq_device_fault() (or synchronizing call)
+ *   returns GPTQ_ERR_TIMEOUT.
+ */
+GPTQ_API gptq_status_t gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                                       const int32_t* g_idx, int64_t d_row, int64_t d_col, int32_t bits,
+                                       int32_t group_size, int32_t out_dtype, void* W_out,
+                                       gptq_stream_t stream);
+
 /* Static English text for a status code. */
 GPTQ_API const char* gptq_status_string(gptq_status_t status);
 

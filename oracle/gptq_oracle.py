@@ -429,6 +429,31 @@ def dequantize(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
     return s * (np.asarray(codes, dtype=np.float64) - z)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), returned
+    as float32: keep the top 16 bits after adding half an ulp of bf16."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
+def dequantize_as(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray, g_idx: np.ndarray,
+                  dtype: str) -> np.ndarray:
+    """Dense weights as stored in `dtype` ("fp32", "fp16", "bf16"): the
+    product scale * (code - zero) formed in fp32 (the difference is a small
+    exact integer), then rounded to nearest in the storage type."""
+    s = np.asarray(scales, dtype=np.float32)[g_idx].T
+    dq = (np.asarray(codes, dtype=np.int64) - np.asarray(zeros, dtype=np.int64)[g_idx].T).astype(np.float32)
+    w = (s * dq).astype(np.float32)
+    if dtype == "fp32":
+        return w
+    if dtype == "fp16":
+        return w.astype(np.float16).astype(np.float32)
+    if dtype == "bf16":
+        return round_bf16(w)
+    raise ValueError(dtype)
+
+
 def recon_error(W: np.ndarray, Q: np.ndarray, S: np.ndarray) -> float:
     """||(W - Q) X||_F^2 = tr((W - Q) S (W - Q)^T) with the undamped S = X X^T."""
     D = np.asarray(W, dtype=np.float64) - np.asarray(Q, dtype=np.float64)

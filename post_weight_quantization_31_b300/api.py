@@ -189,6 +189,23 @@ def unpack(qweight: torch.Tensor, qzeros: torch.Tensor, d_row: int, d_col: int, 
     return codes, zeros
 
 
+_OUT_DT = {torch.float32: _lib.W_FP32, torch.bfloat16: _lib.W_BF16, torch.float16: _lib.W_FP16}
+
+
+def dequantize(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+               g_idx: torch.Tensor, d_row: int, d_col: int, bits: int, group_size: int,
+               dtype=torch.float16, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense weights [d_row, d_col] (original column order) from the packed layer."""
+    lib = _lib.load()
+    if dtype not in _OUT_DT:
+        raise ValueError("dtype must be fp32, bf16 or fp16")
+    out = torch.empty((d_row, d_col), dtype=dtype, device=qweight.device) if out is None else out
+    _check(lib.gptq_dequantize(qweight.data_ptr(), qzeros.data_ptr(), scales.data_ptr(),
+                               g_idx.data_ptr(), d_row, d_col, bits, group_size, _OUT_DT[dtype],
+                               out.data_ptr(), _stream()), "gptq_dequantize")
+    return out
+
+
 def device_fault() -> None:
     _check(_lib.load().gptq_device_fault(_stream()), "gptq_device_fault")
 

@@ -41,6 +41,9 @@ gptq_status_t launch_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_
                           int bits, int n_groups, int32_t* qweight, int32_t* qzeros, cudaStream_t st);
 gptq_status_t launch_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row, int64_t d_col,
                             int bits, int n_groups, uint8_t* codes, uint8_t* zeros, cudaStream_t st);
+gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                             const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits, int n_groups,
+                             int out_dtype, void* W, cudaStream_t st);
 
 namespace {
 
@@ -201,6 +204,24 @@ gptq_status_t gptq_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t
   if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
   return launch_unpack(qweight, qzeros, d_row, d_col, bits, n_groups_of(group_size, d_col), codes, zeros,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status_t gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                              const int32_t* g_idx, int64_t d_row, int64_t d_col, int32_t bits,
+                              int32_t group_size, int32_t out_dtype, void* W_out, gptq_stream_t stream) {
+  if (!qweight || !qzeros || !scales || !g_idx || !W_out) return GPTQ_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || d_row < 32 || d_row % 32 != 0 || d_col < 32 || d_col % 32 != 0)
+    return GPTQ_ERR_INVALID_ARG;
+  if (group_size != -1 && (group_size <= 0 || d_col % group_size != 0)) return GPTQ_ERR_INVALID_ARG;
+  if (out_dtype != GPTQ_W_FP32 && out_dtype != GPTQ_W_BF16 && out_dtype != GPTQ_W_FP16)
+    return GPTQ_ERR_INVALID_ARG;
+  if (d_row * d_col > (int64_t(1) << 31) - 1) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(qweight, 16) || !aligned(qzeros, 4) || !aligned(scales, 4) || !aligned(g_idx, 16) ||
+      !aligned(W_out, 16))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  return launch_dequant(qweight, qzeros, scales, g_idx, d_row, d_col, bits, n_groups_of(group_size, d_col),
+                        out_dtype, W_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gptq_status_string(gptq_status_t s) {

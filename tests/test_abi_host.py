@@ -160,3 +160,18 @@ def test_syrk_schedule_covers_all_tiles(lib, d):
 def test_syrk_schedule_small_token_count(lib):
     s = schedule(lib, 512, 2048, 148)
     assert s["ks"] <= 2048 // 64 // 8
+
+
+def test_dequantize_rejects_bad_args(lib):
+    ok = dict(qw=FAKE, qz=FAKE, sc=FAKE, gi=FAKE, d_row=64, d_col=256, bits=4, gs=128, dt=2, out=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.gptq_dequantize(a["qw"], a["qz"], a["sc"], a["gi"], a["d_row"], a["d_col"], a["bits"],
+                                   a["gs"], a["dt"], a["out"], None)
+    assert call(bits=5) == 1
+    assert call(d_col=250) == 1
+    assert call(gs=96) == 1
+    assert call(dt=7) == 1
+    assert call(out=FAKE + 8) == 1      # output must be 16-byte aligned
+    assert call(qw=0) == 1

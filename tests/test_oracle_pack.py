@@ -71,3 +71,26 @@ def test_roundtrip_exhaustive(bits):
 def test_rejects_out_of_range_code():
     with pytest.raises(ValueError):
         O.pack_qweight(np.array([[16] + [0] * 7]), 4)
+
+
+def test_dequantize_worked_example():
+    """Two rows, four columns, two groups scattered by g_idx (act-order):
+    W[r, c] = s[g, r] * (q[r, c] - z[g, r]) with g = g_idx[c], by hand."""
+    codes = np.array([[3, 0, 15, 8], [1, 2, 7, 9]])
+    scales = np.array([[0.5, 0.25], [2.0, 0.125]])      # [G=2, d_row=2]
+    zeros = np.array([[8, 4], [7, 1]])
+    g_idx = np.array([1, 0, 0, 1])
+    want = np.array([[2.0 * (3 - 7), 0.5 * (0 - 8), 0.5 * (15 - 8), 2.0 * (8 - 7)],
+                     [0.125 * (1 - 1), 0.25 * (2 - 4), 0.25 * (7 - 4), 0.125 * (9 - 1)]])
+    np.testing.assert_array_equal(O.dequantize(codes, scales, zeros, g_idx), want)
+    for dt in ("fp32", "fp16", "bf16"):
+        np.testing.assert_array_equal(O.dequantize_as(codes, scales, zeros, g_idx, dt), want)
+
+
+def test_bf16_rounding_ties_to_even():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to the even mantissa (1.0);
+    # 1 + 3*2^-8 is halfway between 1 + 2^-7 and 1 + 2^-6: ties to 1 + 2^-6.
+    x = np.array([1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -8 + 2.0 ** -20, -(1 + 2.0 ** -8)],
+                 dtype=np.float32)
+    np.testing.assert_array_equal(O.round_bf16(x), np.array([1.0, 1 + 2.0 ** -6, 1 + 2.0 ** -7, -1.0],
+                                                            dtype=np.float32))
