@@ -370,6 +370,73 @@ def run_dequant_only(args) -> dict:
             "dequant": res}
 
 
+def run_dqgemm_only(args) -> dict:
+    """--dqgemm-only MxNxK[,MxNxK...]: Y [M, N] = X [M, K] (fp16) times a
+    random packed 4-bit g128 layer [N, K] (packed by the library),
+    dequantized on the fly.  Algorithmic bytes: packed words, zeros, scales,
+    g_idx and X read once, Y written once.  Each case also times cuBLAS
+    (torch.matmul) on the same layer dequantized to dense fp16, for
+    comparison."""
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib
+    build_lib.build()
+    peaks = measured_peaks()
+    hbm, tc = float(peaks.get("hbm_gbs", 6400.0)), float(peaks.get("bf16_tflops", 1800.0))
+    stream = torch.cuda.current_stream()
+    flush = torch.ones(64 << 20, dtype=torch.float32, device="cuda")
+    reps = max(1, args.dequant_reps)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        ms = []
+        for _ in range(reps):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    cases = []
+    for shape in args.dqgemm_only.lower().split(","):
+        M, N, K = (int(v) for v in shape.split("x"))
+        bits, gs = 4, 128
+        G = K // gs
+        gen = torch.Generator(device="cuda").manual_seed(7)
+        codes = torch.randint(0, 1 << bits, (N, K), dtype=torch.uint8, device="cuda", generator=gen)
+        zeros = torch.randint(0, 1 << bits, (G, N), dtype=torch.uint8, device="cuda", generator=gen)
+        qweight, qzeros = api.pack(codes, zeros, bits, gs)
+        del codes
+        scales = torch.rand((G, N), device="cuda", generator=gen) * 0.02 + 1e-3
+        g_idx = (torch.arange(K, device="cuda", dtype=torch.int32) // gs).contiguous()
+        X = torch.randn((M, K), device="cuda", generator=gen).half()
+        Y = torch.empty((M, N), device="cuda")
+        t = timed(lambda: api.dequant_matmul(X, qweight, qzeros, scales, g_idx, N, K, bits, gs, out=Y))
+        case = {"M": M, "N": N, "K": K, "us": round(t * 1e3, 2)}
+        if args.dqgemm_compare:
+            Wd = api.dequantize(qweight, qzeros, scales, g_idx, N, K, bits, gs, dtype=torch.float16)
+            case["cublas_dense_fp16_us"] = round(timed(lambda: torch.matmul(X, Wd.t())) * 1e3, 2)
+            del Wd
+        nbytes = sum(x.numel() * x.element_size() for x in (qweight, qzeros, scales, g_idx, X, Y))
+        gbs = nbytes / (t * 1e-3) / 1e9
+        tfl = 2.0 * M * N * K / (t * 1e-3) / 1e12
+        case["roofline"] = {"hbm": {"achieved": round(gbs, 1), "frac": round(gbs / hbm, 4)},
+                            "tensor": {"achieved": round(tfl, 1), "frac": round(tfl / tc, 4)}}
+        cases.append(case)
+        del qweight, qzeros, scales, X, Y
+        torch.cuda.empty_cache()
+    return {"metric": "fused dequant-GEMM time (us)", "value": cases[0]["us"], "unit": "us",
+            "n_gpus": 1, "higher_is_better": False, "data": "synthetic", "reps": reps,
+            "config": {"workload": "Y[M,N] = X[M,K] fp16 x packed 4-bit g128 W[N,K]^T, per case",
+                       "l2": "flushed by a 256 MB read before each launch"},
+            "peaks": {"hbm_gbs": hbm, "bf16_tflops": tc, "note": f"{peaks['source']} copy bandwidth and "
+                                                                 "bf16 dense burst"},
+            "cases": cases}
+
+
 # ---------------------------------------------------------------- oracle arm
 def _blas_threads() -> int:
     try:
@@ -469,6 +536,10 @@ def main() -> None:
                     help="timed launches of the packed-layer dequantization (0: skip)")
     ap.add_argument("--dequant-only", default=None, metavar="ROWSxCOLS",
                     help="time only the dequantization of a packed layer of this shape")
+    ap.add_argument("--dqgemm-only", default=None, metavar="MxNxK[,MxNxK...]",
+                    help="time only the fused dequant-GEMM for these sizes")
+    ap.add_argument("--dqgemm-compare", action="store_true",
+                    help="with --dqgemm-only: also time cuBLAS on the dense fp16 weights")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     ap.add_argument("--syrk-traffic", type=float, default=None,
                     help="DRAM bytes per Hessian launch from an ncu capture")
@@ -483,6 +554,8 @@ def main() -> None:
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.dequant_only:
         line = run_dequant_only(args)
+    elif args.dqgemm_only:
+        line = run_dqgemm_only(args)
     elif args.impl == "reference":
         line = run_reference(args, rank)
     else:

@@ -261,6 +261,33 @@ GPTQ_API gptq_status_t gptq_dequantize(const int32_t* qweight, const int32_t* qz
                                        int32_t group_size, int32_t out_dtype, void* W_out,
                                        gptq_stream_t stream);
 
+/*
+ * Y = X · Wᵀ with W the packed layer, dequantized on the fly: the matmul a
+ * GPTQ layer runs at inference, unpacking the codes to 16-bit weights and
+ * multiplying ([G] §4.3), with the desc_act column order resolved through
+ * g_idx ([G] §5.2).  W[n][k] = scales[g][n]·(code[n][k] − zero[g][n]),
+ * g = g_idx[k], formed in fp32 and rounded to X's type (the same values
+ * gptq_dequantize writes for that type); the products are summed in fp32 on
+ * the tensor cores.  The order of the sums is the kernel's: results agree
+ * with an exact product of the same operands to within
+ * (d_col + 148)·2⁻²³·Σ_k |X[m][k]·W[n][k]|.
+ *   X        [M, ldx] of x_dtype (GPTQ_W_FP16 or GPTQ_W_BF16), the first
+ *            d_col entries of each row used; 16-byte aligned, ldx % 8 == 0.
+ *   qweight, qzeros, scales, g_idx   as for gptq_dequantize (qweight,
+ *            scales and g_idx 16-byte aligned).  d_row = output features
+ *            (N), d_col = input features (K).
+ *   Y        fp32 [M, d_row], overwritten.
+ *   d_row % 32 == 0, d_col % 64 == 0, M >= 1, group_size as in gptq_pack.
+ *   All pointers are device memory owned by the caller.  Asynchronous;
+ *   GPTQ_ERR_INVALID_ARG for bad sizes, types or alignment.  Internal waits
+ *   are bounded as for gptq_dequantize.
+ */
+GPTQ_API gptq_status_t gptq_dequant_matmul(const void* X, int32_t x_dtype, int64_t M, int64_t ldx,
+                                           const int32_t* qweight, const int32_t* qzeros,
+                                           const float* scales, const int32_t* g_idx, int64_t d_row,
+                                           int64_t d_col, int32_t bits, int32_t group_size, float* Y,
+                                           gptq_stream_t stream);
+
 /* Static English text for a status code. */
 GPTQ_API const char* gptq_status_string(gptq_status_t status);
 

@@ -9,5 +9,5 @@ from .gptq_oracle import (OracleConfig, LayerResult, as_config, hessian_sum,  # 
                           hessian_columns, damped_hessian, act_order, act_order_diag, hinv_upper,
                           hinv_upper_reverse, prepare, quant_params, quantize_codes,
                           dequantize_codes, column_loop, group_index, quantize_layer,
-                          rtn, dequantize, dequantize_as, round_bf16, recon_error, pack_qweight, unpack_qweight,
+                          rtn, dequantize, dequantize_as, dequant_matmul, round_bf16, recon_error, pack_qweight, unpack_qweight,
                           pack_qzeros, unpack_qzeros, packed_bytes, maxq_of)

@@ -454,6 +454,15 @@ def dequantize_as(codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray, g_id
     raise ValueError(dtype)
 
 
+def dequant_matmul(X: np.ndarray, codes: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+                   g_idx: np.ndarray, dtype: str) -> np.ndarray:
+    """Y = X · Wᵀ in fp64, W the dequantized layer as stored in `dtype`
+    ([G] §4.3: the codes are unpacked to 16-bit weights, then multiplied).
+    X holds the values of the 16-bit activations."""
+    W = dequantize_as(codes, scales, zeros, g_idx, dtype).astype(np.float64)
+    return np.asarray(X, dtype=np.float64) @ W.T
+
+
 def recon_error(W: np.ndarray, Q: np.ndarray, S: np.ndarray) -> float:
     """||(W - Q) X||_F^2 = tr((W - Q) S (W - Q)^T) with the undamped S = X X^T."""
     D = np.asarray(W, dtype=np.float64) - np.asarray(Q, dtype=np.float64)

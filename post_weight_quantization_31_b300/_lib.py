@@ -49,6 +49,8 @@ SIGNATURES = {
     "gptq_pack": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp]),
     "gptq_unpack": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp]),
     "gptq_dequantize": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp]),
+    "gptq_dequant_matmul": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32,
+                                   _vp, _vp]),
     "gptq_status_string": (ctypes.c_char_p, [_i32]),
     "gptq_device_fault": (_i32, [_vp]),
     "gptq_launch_count": (ctypes.c_uint64, []),

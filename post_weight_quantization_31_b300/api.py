@@ -206,6 +206,22 @@ def dequantize(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor
     return out
 
 
+def dequant_matmul(X: torch.Tensor, qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+                   g_idx: torch.Tensor, d_row: int, d_col: int, bits: int, group_size: int,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """Y [M, d_row] fp32 = X [M, d_col] (fp16 or bf16) times the packed
+    layer's dequantized weights, transposed."""
+    lib = _lib.load()
+    if X.dtype not in (torch.float16, torch.bfloat16) or X.dim() != 2 or X.stride(1) != 1:
+        raise ValueError("X must be a 2-D fp16/bf16 tensor with unit column stride")
+    M = X.shape[0]
+    out = torch.empty((M, d_row), dtype=torch.float32, device=X.device) if out is None else out
+    _check(lib.gptq_dequant_matmul(X.data_ptr(), _OUT_DT[X.dtype], M, X.stride(0), qweight.data_ptr(),
+                                   qzeros.data_ptr(), scales.data_ptr(), g_idx.data_ptr(), d_row, d_col,
+                                   bits, group_size, out.data_ptr(), _stream()), "gptq_dequant_matmul")
+    return out
+
+
 def device_fault() -> None:
     _check(_lib.load().gptq_device_fault(_stream()), "gptq_device_fault")
 

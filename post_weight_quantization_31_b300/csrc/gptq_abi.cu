@@ -44,6 +44,10 @@ gptq_status_t launch_unpack(const int32_t* qweight, const int32_t* qzeros, int64
 gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, const float* scales,
                              const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits, int n_groups,
                              int out_dtype, void* W, cudaStream_t st);
+gptq_status_t launch_dequant_matmul(const void* X, int x_dtype, int64_t M, int64_t ldx, const int32_t* qweight,
+                                    const int32_t* qzeros, const float* scales, const int32_t* g_idx,
+                                    int64_t d_row, int64_t d_col, int bits, int n_groups, float* Y,
+                                    cudaStream_t st);
 
 namespace {
 
@@ -222,6 +226,27 @@ gptq_status_t gptq_dequantize(const int32_t* qweight, const int32_t* qzeros, con
   if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
   return launch_dequant(qweight, qzeros, scales, g_idx, d_row, d_col, bits, n_groups_of(group_size, d_col),
                         out_dtype, W_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status_t gptq_dequant_matmul(const void* X, int32_t x_dtype, int64_t M, int64_t ldx,
+                                  const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                                  const int32_t* g_idx, int64_t d_row, int64_t d_col, int32_t bits,
+                                  int32_t group_size, float* Y, gptq_stream_t stream) {
+  if (!X || !qweight || !qzeros || !scales || !g_idx || !Y) return GPTQ_ERR_INVALID_ARG;
+  if (x_dtype != GPTQ_W_FP16 && x_dtype != GPTQ_W_BF16) return GPTQ_ERR_INVALID_ARG;
+  if (!bits_ok(bits) || d_row < 32 || d_row % 32 != 0 || d_col < 64 || d_col % 64 != 0)
+    return GPTQ_ERR_INVALID_ARG;
+  if (group_size != -1 && (group_size <= 0 || d_col % group_size != 0)) return GPTQ_ERR_INVALID_ARG;
+  if (M < 1 || ldx < d_col || ldx % 8 != 0) return GPTQ_ERR_INVALID_ARG;
+  if (M * d_row > (int64_t(1) << 31) - 1 || d_row * d_col > (int64_t(1) << 31) - 1 ||
+      M * ldx > (int64_t(1) << 40))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || !aligned(qweight, 16) || !aligned(g_idx, 16) || !aligned(qzeros, 4) ||
+      !aligned(scales, 16) || !aligned(Y, 4))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  return launch_dequant_matmul(X, x_dtype, M, ldx, qweight, qzeros, scales, g_idx, d_row, d_col, bits,
+                               n_groups_of(group_size, d_col), Y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gptq_status_string(gptq_status_t s) {

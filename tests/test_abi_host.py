@@ -175,3 +175,22 @@ def test_dequantize_rejects_bad_args(lib):
     assert call(dt=7) == 1
     assert call(out=FAKE + 8) == 1      # output must be 16-byte aligned
     assert call(qw=0) == 1
+
+
+def test_dequant_matmul_rejects_bad_args(lib):
+    ok = dict(X=FAKE, dt=2, M=16, ldx=256, qw=FAKE, qz=FAKE, sc=FAKE, gi=FAKE, d_row=128, d_col=256,
+              bits=4, gs=128, Y=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.gptq_dequant_matmul(a["X"], a["dt"], a["M"], a["ldx"], a["qw"], a["qz"], a["sc"],
+                                       a["gi"], a["d_row"], a["d_col"], a["bits"], a["gs"], a["Y"], None)
+    assert call(dt=0) == 1              # fp32 activations are not a tensor-core operand here
+    assert call(M=0) == 1
+    assert call(ldx=200) == 1           # ldx < d_col
+    assert call(ldx=260) == 1           # ldx % 8 != 0
+    assert call(d_col=224) == 1         # d_col % 64 != 0
+    assert call(X=FAKE + 8) == 1        # X must be 16-byte aligned
+    assert call(gi=FAKE + 4) == 1       # g_idx must be 16-byte aligned
+    assert call(sc=FAKE + 4) == 1       # scales must be 16-byte aligned
+    assert call(Y=0) == 1

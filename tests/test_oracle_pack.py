@@ -94,3 +94,24 @@ def test_bf16_rounding_ties_to_even():
                  dtype=np.float32)
     np.testing.assert_array_equal(O.round_bf16(x), np.array([1.0, 1 + 2.0 ** -6, 1 + 2.0 ** -7, -1.0],
                                                             dtype=np.float32))
+
+
+def test_dequant_matmul_brute_force():
+    """Y[m][n] = sum_k X[m][k] * W[n][k] with W[n][k] = s[g_k][n] * (q[n][k] - z[g_k][n])
+    stored in fp32, by loops."""
+    rng = np.random.Generator(np.random.PCG64(4))
+    M, N, K, bits = 3, 4, 6, 3
+    codes = rng.integers(0, 1 << bits, size=(N, K))
+    zeros = rng.integers(0, 1 << bits, size=(2, N))
+    scales = rng.uniform(0.1, 1.0, size=(2, N)).astype(np.float32)
+    g_idx = np.array([1, 0, 1, 1, 0, 0])
+    X = rng.standard_normal((M, K)).astype(np.float16).astype(np.float64)
+    want = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            for k in range(K):
+                g = g_idx[k]
+                w = np.float32(scales[g, n]) * np.float32(codes[n, k] - zeros[g, n])  # W stored in fp32
+                want[m, n] += X[m, k] * float(w)
+    got = O.dequant_matmul(X, codes, scales, zeros, g_idx, "fp32")
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
