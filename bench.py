@@ -370,6 +370,57 @@ def run_dequant_only(args) -> dict:
             "dequant": res}
 
 
+def run_sweep(args) -> dict:
+    """--sweep BITS:GS[:act],...: the bench step (S = 0, accumulate, prepare,
+    quantize, pack) on the bench workload for other quantizer settings
+    (group_size -1 = one group per row; act = desc_act on).  Timing as for
+    the main line: W warm-up steps, then K steps between CUDA events."""
+    import dataclasses
+
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    inp = make_inputs()
+    X = torch.from_numpy(inp.X).to(dev)
+    W = torch.from_numpy(inp.W).to(torch.bfloat16).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    cases = []
+    for spec in args.sweep.split(","):
+        parts = spec.split(":")
+        bits, gs = int(parts[0]), int(parts[1])
+        act = len(parts) > 2 and parts[2] == "act"
+        cfg = dataclasses.replace(inp.cfg, bits=bits, group_size=gs, desc_act=act)
+        solver = api.LayerSolver(D, D, cfg, device=dev, exact_diag=False)
+
+        def step():
+            solver.reset()
+            solver.accumulate(X)
+            solver.prepare()
+            solver.quantize(W)
+            solver.pack()
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize(dev)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = t0.elapsed_time(t1) / args.steps
+        cases.append({"bits": bits, "group_size": gs, "desc_act": act, "ms_per_step": round(ms, 4),
+                      "value": round(D * D / (ms * 1e-3) / 1e6, 3)})
+        del solver
+        torch.cuda.empty_cache()
+    return {"metric": METRIC.split(" (")[0] + " (4096x4096, per quantizer setting)", "value": cases[0]["value"],
+            "unit": "Mweights/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+            "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": WORKLOAD.split("; 4-bit")[0] + "; settings per case",
+                       "l2": "inputs larger than L2 (X is 2.15 GB)"},
+            "cases": cases}
+
+
 def run_dqgemm_only(args) -> dict:
     """--dqgemm-only MxNxK[,MxNxK...]: Y [M, N] = X [M, K] (fp16) times a
     random packed 4-bit g128 layer [N, K] (packed by the library),
@@ -536,6 +587,8 @@ def main() -> None:
                     help="timed launches of the packed-layer dequantization (0: skip)")
     ap.add_argument("--dequant-only", default=None, metavar="ROWSxCOLS",
                     help="time only the dequantization of a packed layer of this shape")
+    ap.add_argument("--sweep", default=None, metavar="BITS:GS[:act],...",
+                    help="time the bench step for other quantizer settings")
     ap.add_argument("--dqgemm-only", default=None, metavar="MxNxK[,MxNxK...]",
                     help="time only the fused dequant-GEMM for these sizes")
     ap.add_argument("--dqgemm-compare", action="store_true",
@@ -556,6 +609,8 @@ def main() -> None:
         line = run_dequant_only(args)
     elif args.dqgemm_only:
         line = run_dqgemm_only(args)
+    elif args.sweep:
+        line = run_sweep(args)
     elif args.impl == "reference":
         line = run_reference(args, rank)
     else:

@@ -110,3 +110,28 @@ def test_dequantize_full_size_sampled_rows():
     assert np.array_equal(codes_o, codes.cpu().numpy()[rows])
     want = O.dequantize_as(codes_o, scales_h[:, rows], zeros_o[:, rows], g_idx_h, "fp16")
     assert np.array_equal(got, want)
+
+
+def test_container_round_trip_of_a_solved_layer(tmp_path):
+    """A layer solved on the GPU, saved with quantize_config.json + safetensors,
+    loaded back and dequantized: the same dense weights as before saving."""
+    import torch
+    from post_weight_quantization_31_b300 import api, container
+    from post_weight_quantization_31_b300 import workloads as wl
+    cfg = wl.QuantConfig(bits=4, group_size=64, desc_act=True)
+    d_row, d_col = 64, 256
+    W = torch.from_numpy(wl.make_weight(d_row, d_col, seed=3)).cuda()
+    X = torch.from_numpy(wl.make_activations(d_col, 1024, seed=4)).cuda()
+    solver = api.LayerSolver(d_row, d_col, cfg)
+    solver.reset()
+    res = solver.solve(W, X)
+    before = api.dequantize(res.qweight, res.qzeros, res.scales, res.g_idx, d_row, d_col, 4, 64,
+                            dtype=torch.float32)
+    container.save_quantized(str(tmp_path), {"layer": res}, cfg)
+    layers, cfg2 = container.load_quantized(str(tmp_path))
+    assert cfg2 == cfg
+    L = {k: torch.from_numpy(v).cuda() for k, v in layers["layer"].items()}
+    after = api.dequantize(L["qweight"], L["qzeros"], L["scales"], L["g_idx"], d_row, d_col, 4, 64,
+                           dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(before, after)
