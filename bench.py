@@ -168,6 +168,54 @@ def job_throughput(units_per_rank: float, steps: int, world: int, seconds: float
 
 
 # ---------------------------------------------------------------- inputs
+def fp32_alu_peak_tflops(sms: int = 148, clock_ghz: float = 2.032) -> float:
+    """FP32 FFMA peak: SMs x 128 lanes x 2 flop x the maximum SM clock."""
+    return sms * 128 * 2 * clock_ghz * 1e9 / 1e12
+
+
+def phase_rooflines(ph_ms: dict, d_row: int, d_col: int, bits: int, group_size: int,
+                    peaks: dict, block: int = 128) -> dict:
+    """Roofline fraction of each solve phase from its CUDA-event time and its
+    algorithmic work:
+      prepare   2·d³/3 flop (the reverse-route Cholesky with its inverse)
+                against the FP32 FFMA peak (the panels are FP32 ALU work; the
+                trailing updates run as 3xTF32 on the tensor cores);
+      quantize  the trailing updates' d_row·d_col·(d_col − B) flop against
+                the 3xTF32 rate (a third of the TF32 peak, TF32 = bf16 / 2
+                nominal); the column loop inside the same phase moves
+                read W (2 B) + codes (bits/8 B) + scale/zero (5 B per group
+                element) per weight, reported against HBM;
+      pack      1 + bits/8 B per weight against HBM."""
+    hbm = float(peaks.get("hbm_gbs", 6400.0))
+    tf32_3x = float(peaks.get("bf16_tflops", 1800.0)) / 2.0 / 3.0
+    alu = fp32_alu_peak_tflops()
+    W = float(d_row) * d_col
+    G = 1 if group_size == -1 else d_col // group_size
+    out = {}
+    t = ph_ms.get("prepare")
+    if t:
+        a = 2.0 * d_col ** 3 / 3.0 / (t * 1e-3) / 1e12
+        out["prepare"] = {"bound": "alu", "achieved": round(a, 2), "peak": round(alu, 1),
+                          "unit": "TFLOP/s", "frac": round(a / alu, 4)}
+    t = ph_ms.get("quantize")
+    if t:
+        a = W * max(d_col - block, 0) / (t * 1e-3) / 1e12
+        col_bytes = W * (2.0 + bits / 8.0) + 5.0 * G * d_row
+        b = col_bytes / (t * 1e-3) / 1e9
+        out["quantize"] = {"bound": "tensor", "achieved": round(a, 2), "peak": round(tf32_3x, 1),
+                           "unit": "TFLOP/s", "frac": round(a / tf32_3x, 4),
+                           "column_loop_bytes": int(col_bytes), "column_loop_gbs": round(b, 1),
+                           "column_loop_frac_of_hbm": round(b / hbm, 4)}
+    t = ph_ms.get("pack")
+    if t:
+        b = W * (1.0 + bits / 8.0) / (t * 1e-3) / 1e9
+        out["pack"] = {"bound": "hbm", "achieved": round(b, 1), "peak": hbm, "unit": "GB/s",
+                       "frac": round(b / hbm, 4)}
+    out["peak_note"] = (f"{peaks.get('source', 'fallback')} HBM and bf16 burst; TF32 = bf16/2 and FP32 "
+                        f"FFMA = 148 x 128 x 2 x 2.032 GHz, both nominal")
+    return out
+
+
 def make_inputs():
     from post_weight_quantization_31_b300 import workloads as wl
     return wl.attn_proj_7b(seed=1002, n_tok=N_TOK, d=D)
@@ -289,6 +337,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "l2": "inputs larger than L2 (X is 2.15 GB)",
                    "parallelism": f"one independent layer per GPU x{world}"},
         "phases_ms": {k: round(v, 4) for k, v in ph.items()},
+        "phases_roofline": phase_rooflines(ph, D, D, cfg.bits, cfg.group_size, peaks),
+        "solve_only": {"value": round(D * D / ((ph["prepare"] + ph["quantize"] + ph["pack"]) * 1e-3) / 1e6, 3),
+                       "unit": "Mweights/s",
+                       "note": "prepare + quantize + pack with H given, from the same timed steps"},
         "gpu_launches": int(launches),
         "roofline": roof,
         "clocks": clk.summary(),
@@ -368,6 +420,91 @@ def run_dequant_only(args) -> dict:
             "config": {"workload": f"packed {d_row}x{d_col} 4-bit g128 layer -> bf16, no act-order",
                        "l2": "flushed by a 256 MB read before each launch"},
             "dequant": res}
+
+
+LAYER_SET_SITES = ("qkv", "o", "gate_up", "down")
+
+
+def run_layer_set(args) -> dict:
+    """--layer-set L: the 7B-shaped layer set, L decoder layers x 4 input
+    sites (q|k|v rows stacked on one X, o, gate|up stacked, down; 4-bit sym
+    g128, 65536 tokens per site).  Each site: S = 0, accumulate, prepare,
+    quantize, pack.  The inputs of one decoder layer are generated once (the
+    seeded generators of workloads.py) and reused for every layer: each
+    layer does the same work on data of the same distribution.
+      sequential: one stream, layer after layer, site after site;
+      concurrent: the four sites of each layer on four streams (one host
+      thread each; the library's status reads block only their own stream).
+    Both are timed between CUDA events / device synchronizations."""
+    import threading
+
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib, workloads as wl
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    L = int(args.layer_set)
+    sites = {}
+    for site in LAYER_SET_SITES:
+        inp = wl.decoder_site_7b(site, layer=0)
+        d_row, d_col = inp.W.shape
+        sites[site] = dict(X=torch.from_numpy(inp.X).to(dev),
+                           W=torch.from_numpy(inp.W).to(torch.bfloat16).to(dev),
+                           solver=api.LayerSolver(d_row, d_col, inp.cfg, device=dev), weights=d_row * d_col)
+    weights_per_layer = sum(v["weights"] for v in sites.values())
+
+    def solve(site):
+        v = sites[site]
+        v["solver"].reset()
+        v["solver"].accumulate(v["X"])
+        v["solver"].prepare()
+        v["solver"].quantize(v["W"])
+        v["solver"].pack()
+
+    for site in LAYER_SET_SITES:          # warm-up
+        solve(site)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(L):
+        for site in LAYER_SET_SITES:
+            solve(site)
+    torch.cuda.synchronize(dev)
+    t_seq = time.perf_counter() - t0
+
+    streams = {site: torch.cuda.Stream(dev) for site in LAYER_SET_SITES}
+    errors = []
+
+    def worker(site):
+        try:
+            with torch.cuda.stream(streams[site]):
+                for _ in range(L):
+                    solve(site)
+            streams[site].synchronize()
+        except Exception as e:  # reported below; the other threads finish their layers
+            errors.append(f"{site}: {e}")
+
+    threads = [threading.Thread(target=worker, args=(site,)) for site in LAYER_SET_SITES]
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize(dev)
+    t_con = time.perf_counter() - t0
+    if errors:
+        raise RuntimeError("; ".join(errors))
+    return {"metric": "7B-shaped layer set: seconds per 32 decoder layers", "value": round(t_seq * 32 / L, 3),
+            "unit": "s", "n_gpus": 1, "higher_is_better": False, "data": "synthetic",
+            "config": {"workload": "32 x {q|k|v 12288x4096, o 4096x4096, gate|up 22016x4096, down 4096x11008} "
+                                   "bf16 N(0,0.02^2); X fp16 65536 tokens per site, N(0,1), 1% channels "
+                                   "x U[10,50]; 4-bit sym g128, damp 0.01, desc_act off",
+                       "layers_timed": L, "inputs": "one decoder layer's inputs, reused for every layer"},
+            "sequential_s": round(t_seq, 4), "concurrent_s": round(t_con, 4),
+            "sequential_s_per_32_layers": round(t_seq * 32 / L, 3),
+            "concurrent_s_per_32_layers": round(t_con * 32 / L, 3),
+            "weights_per_layer": int(weights_per_layer),
+            "sequential_mweights_s": round(weights_per_layer * L / t_seq / 1e6, 1),
+            "concurrent_mweights_s": round(weights_per_layer * L / t_con / 1e6, 1)}
 
 
 def run_sweep(args) -> dict:
@@ -587,6 +724,8 @@ def main() -> None:
                     help="timed launches of the packed-layer dequantization (0: skip)")
     ap.add_argument("--dequant-only", default=None, metavar="ROWSxCOLS",
                     help="time only the dequantization of a packed layer of this shape")
+    ap.add_argument("--layer-set", default=None, metavar="L",
+                    help="time L decoder layers of the 7B-shaped layer set (sequential and concurrent)")
     ap.add_argument("--sweep", default=None, metavar="BITS:GS[:act],...",
                     help="time the bench step for other quantizer settings")
     ap.add_argument("--dqgemm-only", default=None, metavar="MxNxK[,MxNxK...]",
@@ -611,6 +750,8 @@ def main() -> None:
         line = run_dqgemm_only(args)
     elif args.sweep:
         line = run_sweep(args)
+    elif args.layer_set:
+        line = run_layer_set(args)
     elif args.impl == "reference":
         line = run_reference(args, rank)
     else:

@@ -46,3 +46,20 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(100, 2, 1, 4.0) == 50.0
+
+
+def test_phase_rooflines_scale_with_time():
+    """Achieved rates are work / time: halving a phase's time doubles its
+    rate; fractions are achieved / peak with the stated peaks."""
+    import bench
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0, "source": "test"}
+    ph = {"prepare": 2.0, "quantize": 1.0, "pack": 0.1}
+    a = bench.phase_rooflines(ph, 4096, 4096, 4, 128, peaks)
+    b = bench.phase_rooflines({k: v / 2 for k, v in ph.items()}, 4096, 4096, 4, 128, peaks)
+    for k in ("prepare", "quantize", "pack"):
+        assert abs(b[k]["achieved"] / a[k]["achieved"] - 2.0) < 1e-3
+        assert abs(a[k]["frac"] - a[k]["achieved"] / a[k]["peak"]) < 1e-3
+    # prepare: 2/3 d^3 flop in 2 ms; pack: 1.5 B/weight in 0.1 ms
+    assert abs(a["prepare"]["achieved"] - 2 * 4096 ** 3 / 3 / 2e-3 / 1e12) < 0.01
+    assert abs(a["pack"]["achieved"] - 4096 * 4096 * 1.5 / 1e-4 / 1e9) < 0.1
+    assert a["quantize"]["peak"] == round(1800.0 / 2 / 3, 1)
