@@ -4,26 +4,27 @@ TEST INFRASTRUCTURE ONLY, like the GPTQ oracle beside it: a plain NumPy fp64
 restatement, imported only by the tests; no product code calls it.
 
 Sources:
-  [A1] "GPTQ vs AWQ" overview (bxzpzcl.cn/news/361031): AWQ takes the RMS of
-       each channel's activations over the calibration data, picks the most
-       active top-k% (5% by default), gives those channels a larger scale so
-       they keep more effective bits, and multiplies back at inference.
-  [A2] "大模型压缩量化技术：GPTQ 与 AWQ 原理详解", §四 (AWQ 原理): the weights
-       of the large-activation channels are multiplied by a factor s > 1
-       before quantization, the matching activations are divided by s at
-       inference so the output is unchanged, and the best factor is
+  [C]  "GPTQ/AWQ量化导出：让大模型在消费级显卡上跑起来", the GPTQ/AWQ comparison:
+       AWQ takes the RMS of each channel's activations over the calibration
+       data, picks the most active top-k% (5% by default), gives those
+       channels a larger scale so they keep more effective bits, and
+       multiplies back at inference.
+  [E]  "大模型压缩量化技术：GPTQ 与 AWQ 原理详解 + Python 实战教程", §四 (AWQ
+       原理): the weights of the large-activation channels are multiplied by a
+       factor s > 1 before quantization, the matching activations are divided
+       by s at inference so the output is unchanged, and the best factor is
        computed from forward statistics only (no Hessian inverse, no
        gradients).
-  [A4] ms-swift evaluation page, AWQ section: states the opposite direction
-       (scale the non-salient channels down, leave the salient ones).  With
-       a per-group min-max grid the two are the same relative scaling: a
-       common factor on a whole row changes no code, so salient x s equals
-       others x 1/s (pinned in the tests with s a power of two, where both
-       are exact in floating point).
+  [S]  "AWQ与GPTQ谁更强？ms-swift量化模块深度评测", AWQ section: states the
+       opposite direction (scale the non-salient channels down, leave the
+       salient ones).  With a per-group min-max grid the two are the same
+       relative scaling: a common factor on a whole row changes no code, so
+       salient x s equals others x 1/s (pinned in the tests with s a power
+       of two, where both are exact in floating point).
 
 Readings (listed in the design notes as R17-R20):
   R17 statistic: RMS over the calibration tokens of each activation channel
-      (W's input channel; [A1] says "output channels", read as the
+      (W's input channel; [C] says "output channels", read as the
       channels of the activations that feed W, the ones divided by s).
   R18 salient set: the ceil(frac * d_col) channels with the largest RMS,
       frac = 0.05; ties keep the lower channel index.
