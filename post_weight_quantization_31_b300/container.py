@@ -19,7 +19,7 @@ nothing else, so:
     multiple of 8 bytes) mapping each tensor name to its dtype, shape and
     [begin, end) byte range in the data section, an optional "__metadata__"
     map of strings, then the data section with the tensors back to back in
-    little-endian order.
+    little-endian order, covering it with no gap.
 
 Host-side file I/O only; nothing here runs on the GPU.
 """
@@ -115,6 +115,10 @@ def read_safetensors(path: str) -> tuple[dict, dict]:
     for (b0, e0, n0), (b1, e1, n1) in zip(spans, spans[1:]):
         if b1 < e0:
             raise ValueError(f"{n0} and {n1} overlap")
+        if b1 > e0:
+            raise ValueError(f"unused bytes between {n0} and {n1}")
+    if spans and (spans[0][0] != 0 or spans[-1][1] != len(data)):
+        raise ValueError("the tensors do not cover the data section exactly")
     return out, metadata
 
 

@@ -68,6 +68,11 @@ def test_rejects_malformed_files(tmp_path):
     with pytest.raises(ValueError):      # overlapping tensors
         C.read_safetensors(_corrupt(tmp_path, {"a": {"dtype": "I32", "shape": [2], "data_offsets": [0, 8]},
                                                "b": {"dtype": "I32", "shape": [2], "data_offsets": [4, 12]}}))
+    with pytest.raises(ValueError):      # a gap between tensors
+        C.read_safetensors(_corrupt(tmp_path, {"a": {"dtype": "I32", "shape": [1], "data_offsets": [0, 4]},
+                                               "b": {"dtype": "I32", "shape": [2], "data_offsets": [8, 16]}}))
+    with pytest.raises(ValueError):      # trailing bytes not covered by any tensor
+        C.read_safetensors(_corrupt(tmp_path, {"a": {"dtype": "I32", "shape": [2], "data_offsets": [0, 8]}}))
     p = tmp_path / "short.safetensors"
     p.write_bytes(struct.pack("<Q", 100) + b"{}")
     with pytest.raises(ValueError):      # header longer than the file
