@@ -103,13 +103,14 @@ def test_dequantize_full_size_sampled_rows():
                          dtype=torch.float16)
     torch.cuda.synchronize()
     rows = np.sort(rng.choice(d_row, size=16, replace=False))
-    qw_h, qz_h = qw.cpu().numpy(), qz.cpu().numpy()
-    zeros_o = O.unpack_qzeros(qz_h, bits, d_row)
     got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy()
-    codes_o = O.unpack_qweight(qw_h[:, rows], bits, d_col)
-    assert np.array_equal(codes_o, codes.cpu().numpy()[rows])
-    want = O.dequantize_as(codes_o, scales_h[:, rows], zeros_o[:, rows], g_idx_h, "fp16")
+    codes_h = codes.cpu().numpy().astype(np.int64)          # the generator's codes
+    zeros_h = zeros.cpu().numpy().astype(np.int64)
+    want = O.dequantize_as(codes_h[rows], scales_h[:, rows], zeros_h[:, rows], g_idx_h, "fp16")
     assert np.array_equal(got, want)
+    # the GPU packing of the sampled rows, against the oracle's packer
+    qw_h = qw.cpu().numpy()
+    assert np.array_equal(qw_h[:, rows], O.pack_qweight(codes_h[rows], bits))
 
 
 def test_container_round_trip_of_a_solved_layer(tmp_path):
