@@ -282,8 +282,7 @@ def _check_blocking(d_col: int, gs: int, blocksize: int) -> None:
             raise ValueError("group starts must coincide with block starts")
 
 
-def column_loop(Wp: np.ndarray, U: np.ndarray, cfg, *, blocksize: int | None = None,
-                forced_codes: np.ndarray | None = None, trace=None):
+def column_loop(Wp: np.ndarray, U: np.ndarray, cfg, *, blocksize: int | None = None, trace=None):
     """Quantize Wp [rows, d_col] (processing order, fp64) with error feedback.
 
     For each block [i1, i2) of `blocksize` columns, for j in the block, per
@@ -297,9 +296,8 @@ def column_loop(Wp: np.ndarray, U: np.ndarray, cfg, *, blocksize: int | None = N
     all remaining weights with one matrix multiply):
       W[:, i2:] -= Err U[i1:i2, i2:].
 
-    forced_codes (same shape as Wp) replaces the code decision with the
-    given codes (replay mode); trace(j, W) is called after column j's
-    in-block update (and, at a block end, after the trailing update).
+    trace(j, W) is called after column j's in-block update (and, at a
+    block end, after the trailing update).
 
     Returns codes int64 [rows, d_col], scales float32 [G, rows],
     zeros int64 [G, rows], Q float64 [rows, d_col] (dequantized values), all
@@ -329,10 +327,7 @@ def column_loop(Wp: np.ndarray, U: np.ndarray, cfg, *, blocksize: int | None = N
                 scales[g], zeros[g] = quant_params(W[:, j:j + gs], cfg.bits, cfg.sym)
                 s, z = scales[g].copy(), zeros[g].copy()
             w = W[:, j]
-            if forced_codes is None:
-                q = quantize_codes(w, s, z, cfg.bits)
-            else:
-                q = np.asarray(forced_codes[:, j], dtype=np.int64)
+            q = quantize_codes(w, s, z, cfg.bits)
             dq = dequantize_codes(q, s, z)
             e = obq_error(w, dq, U[j, j])
             obq_update(W, e, U, j, j + 1, i2)
@@ -371,13 +366,12 @@ class LayerResult:
 
 
 def quantize_layer(W: np.ndarray, S: np.ndarray, n_seen: int, cfg, *,
-                   blocksize: int | None = None, rows=None,
-                   forced_codes: np.ndarray | None = None) -> LayerResult:
+                   blocksize: int | None = None, rows=None) -> LayerResult:
     """The whole solve for one layer (a2 .. a5 minus packing).
 
     W [d_row, d_col] holds the layer's weights (bf16/fp32 values, used in
     fp64).  `rows` restricts the solve to a subset of rows (rows are
-    independent).  forced_codes is given in ORIGINAL column order.
+    independent).
     """
     cfg = as_config(cfg)
     perm, _Hp, U = prepare(S, n_seen, cfg)
@@ -385,9 +379,7 @@ def quantize_layer(W: np.ndarray, S: np.ndarray, n_seen: int, cfg, *,
     if rows is not None:
         W64 = W64[np.asarray(rows)]
     Wp = W64[:, perm]
-    fc = None if forced_codes is None else np.asarray(forced_codes)[:, perm]
-    codes_p, scales, zeros, Q_p = column_loop(Wp, U, cfg, blocksize=blocksize,
-                                              forced_codes=fc)
+    codes_p, scales, zeros, Q_p = column_loop(Wp, U, cfg, blocksize=blocksize)
     codes = np.empty_like(codes_p)
     Q = np.empty_like(Q_p)
     codes[:, perm] = codes_p

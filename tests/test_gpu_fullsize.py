@@ -87,10 +87,6 @@ def check_rows_exact(inp, g, S64, perm, U, rows, code_match=P.CODE_MATCH):
     Qg = O.dequantize(gc, gs, gz, g["g_idx"])
     eg, er = O.recon_error(inp.W[rows], Qg, S64), O.recon_error(inp.W[rows], Q, S64)
     assert abs(eg - er) / er <= P.RECON_RTOL, (eg, er)
-    # forced-code replay: the compensation arithmetic alone
-    _c, rscales, rzeros, _q = O.column_loop(W[:, perm], U, cfg, forced_codes=gc[:, perm])
-    rrel = np.abs(gs.astype(np.float64) - rscales) / np.abs(rscales.astype(np.float64))
-    assert rrel.max() <= P.SCALE_RTOL, rrel.max()
     # packing of the sampled rows, bit-exact
     assert np.array_equal(g["qweight"][:, rows], O.pack_qweight(gc, cfg.bits))
 
