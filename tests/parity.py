@@ -82,14 +82,47 @@ def upstream_groups(g_codes, ref_codes, perm, group_size: int, n_groups: int) ->
     return gstart[:, None] <= first[None, :]
 
 
+# ---------------------------------------------------------------- measuring GPU outputs
+# GPU outputs are measured with the plain NumPy below, never by passing them
+# to the oracle: the oracle only ever sees the inputs.
+
+def dequantized(codes, scales, zeros, g_idx) -> np.ndarray:
+    """s[g][r] * (q[r][c] - z[g][r]) with g = g_idx[c], in fp64."""
+    gi = np.asarray(g_idx, dtype=np.int64)
+    s = np.asarray(scales, dtype=np.float64)[gi].T
+    z = np.asarray(zeros, dtype=np.float64)[gi].T
+    return s * (np.asarray(codes, dtype=np.float64) - z)
+
+
+def output_error(W, Q, S64) -> float:
+    """||(W - Q) X||^2 = tr(D S D^T) with S = X X^T (fp64)."""
+    D = np.asarray(W, dtype=np.float64) - np.asarray(Q, dtype=np.float64)
+    return float(np.einsum("ij,ij->", D @ np.asarray(S64, dtype=np.float64), D))
+
+
+def unpack_columns(words, bits: int, count: int) -> np.ndarray:
+    """Codes of each column of `words` (int32 [n_words, cols]): the column is
+    one LSB-first bit stream of `count` codes of `bits` bits.  Returns
+    int64 [cols, count]."""
+    w = np.ascontiguousarray(np.asarray(words).T).astype("<u4")       # [cols, n_words]
+    bitsarr = np.unpackbits(w.view(np.uint8), axis=1, bitorder="little")[:, :count * bits]
+    weights = (1 << np.arange(bits, dtype=np.int64))
+    return bitsarr.reshape(w.shape[0], count, bits).astype(np.int64) @ weights
+
+
+def unpack_rows(words, bits: int, count: int) -> np.ndarray:
+    """Codes of each row of `words` (int32 [rows, n_words]), LSB-first."""
+    return unpack_columns(np.asarray(words).T, bits, count)
+
+
 def compare(g: GpuOut, ref: O.LayerResult, W: np.ndarray, S64: np.ndarray, cfg) -> dict:
     """Metrics of a GPU result against the oracle's on the same inputs:
     codes, zeros, reconstruction error, and the scales of the groups
     upstream of any code difference.  The oracle only ever sees the inputs
     the GPU saw, never a GPU output."""
     same = g.codes == ref.codes
-    Qg = O.dequantize(g.codes, g.scales, g.zeros, g.g_idx)
-    eg, er = O.recon_error(W, Qg, S64), O.recon_error(W, ref.Q, S64)
+    eg = output_error(W, dequantized(g.codes, g.scales, g.zeros, g.g_idx), S64)
+    er = O.recon_error(W, ref.Q, S64)
     rows_with_flip = int(np.any(~same, axis=1).sum())
     srel = np.abs(g.scales.astype(np.float64) - ref.scales) / np.abs(ref.scales.astype(np.float64))
     up = upstream_groups(g.codes, ref.codes, ref.perm, cfg.group_size, ref.scales.shape[0])

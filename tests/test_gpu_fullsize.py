@@ -84,11 +84,11 @@ def check_rows_exact(inp, g, S64, perm, U, rows, code_match=P.CODE_MATCH):
     srel = np.abs(gs.astype(np.float64) - scales) / np.abs(scales.astype(np.float64))
     assert srel[up].max() <= P.SCALE_RTOL, srel[up].max()
     assert (gz == zeros).mean() >= code_match
-    Qg = O.dequantize(gc, gs, gz, g["g_idx"])
-    eg, er = O.recon_error(inp.W[rows], Qg, S64), O.recon_error(inp.W[rows], Q, S64)
+    eg = P.output_error(inp.W[rows], P.dequantized(gc, gs, gz, g["g_idx"]), S64)
+    er = O.recon_error(inp.W[rows], Q, S64)
     assert abs(eg - er) / er <= P.RECON_RTOL, (eg, er)
     # packing of the sampled rows, bit-exact
-    assert np.array_equal(g["qweight"][:, rows], O.pack_qweight(gc, cfg.bits))
+    assert np.array_equal(P.unpack_columns(g["qweight"][:, rows], cfg.bits, W.shape[1]), gc)
 
 
 def check_hessian_samples(X, S_gpu, n, seed):
@@ -158,8 +158,8 @@ def test_wide_layer_properties_at_full_tokens(name, make, n_full):
     # codes are valid levels and pack exactly
     assert g["codes"].max() <= (1 << cfg.bits) - 1
     rows = sample_rows(inp.W.shape[0], 8, seed=13)
-    assert np.array_equal(g["qweight"][:, rows], O.pack_qweight(g["codes"][rows].astype(np.int64),
-                                                                cfg.bits))
+    assert np.array_equal(P.unpack_columns(g["qweight"][:, rows], cfg.bits, X.shape[0]),
+                          g["codes"][rows].astype(np.int64))
 
 
 _WIDE_CACHE = {}

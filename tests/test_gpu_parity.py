@@ -95,8 +95,9 @@ def test_tiny_layer_parity():
     inp = wl.tiny_layer()
     g, ref, S64, m = run_case(inp.W, inp.w_dtype, inp.X, inp.cfg)
     P.assert_parity(m)
-    assert np.array_equal(g.qweight, O.pack_qweight(g.codes, inp.cfg.bits))
-    assert np.array_equal(g.qzeros, O.pack_qzeros(g.zeros, inp.cfg.bits))
+    d_row, d_col = inp.W.shape
+    assert np.array_equal(P.unpack_columns(g.qweight, inp.cfg.bits, d_col), g.codes)
+    assert np.array_equal(P.unpack_rows(g.qzeros, inp.cfg.bits, d_row), g.zeros)
 
 
 CASES = [
@@ -123,7 +124,7 @@ def test_layer_parity(d_row, d_col, n_tok, w_dtype, kw):
         W = W.astype(np.float16).astype(np.float32)
     g, ref, S64, m = run_case(W, w_dtype, X, cfg, chunks=2)
     P.assert_parity(m)
-    assert np.array_equal(g.qweight, O.pack_qweight(g.codes, cfg.bits))
+    assert np.array_equal(P.unpack_columns(g.qweight, cfg.bits, W.shape[1]), g.codes)
 
 
 def test_correlated_inputs_quality():
@@ -138,8 +139,7 @@ def test_correlated_inputs_quality():
     S64 = O.hessian_sum(X)
     free = O.quantize_layer(W, S64, X.shape[1], cfg)
     assert np.array_equal(g.perm, free.perm)
-    Qg = O.dequantize(g.codes, g.scales, g.zeros, g.g_idx)
-    eg = O.recon_error(W, Qg, S64)
+    eg = P.output_error(W, P.dequantized(g.codes, g.scales, g.zeros, g.g_idx), S64)
     ef = O.recon_error(W, free.Q, S64)
     assert abs(eg - ef) / ef <= 0.02
     assert eg < O.recon_error(W, O.rtn(W, cfg).Q, S64)
@@ -194,7 +194,7 @@ def test_host_buffer_path_matches_oracle(copy_streams):
     W_host = torch.from_numpy(inp.W).pin_memory()
     out = api.quantize_layer_from_host(W_host, chunks, inp.cfg, copy_streams=copy_streams)
     bits = inp.cfg.bits
-    codes = O.unpack_qweight(out["qweight"].numpy(), bits, d_col)
+    codes = P.unpack_columns(out["qweight"].numpy(), bits, d_col)
     S64 = O.hessian_sum(inp.X)
     ref = O.quantize_layer(inp.W, S64, inp.X.shape[1], inp.cfg)
     assert (codes == ref.codes).mean() >= P.CODE_MATCH
@@ -202,5 +202,5 @@ def test_host_buffer_path_matches_oracle(copy_streams):
     assert np.array_equal(out["g_idx"].numpy(), ref.g_idx)
     srel = np.abs(out["scales"].numpy().astype(np.float64) - ref.scales) / ref.scales
     assert srel.max() <= P.SCALE_RTOL
-    zeros = O.unpack_qzeros(out["qzeros"].numpy(), bits, d_row)
+    zeros = P.unpack_rows(out["qzeros"].numpy(), bits, d_row)
     assert (zeros == ref.zeros).mean() >= P.CODE_MATCH
