@@ -173,8 +173,8 @@ GPTQ_API gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int
  *           GPTQ_ERR_WORKSPACE with no side effect.  Other argument errors
  *           and status codes are those of gptq_prepare_hinv.
  *   The first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Every call, from any thread or stream,
+ *   (cudaGetSymbolAddress, with that device current).  Every call, from any
+ *   thread or stream,
  *   shares the one array and leaves its contents behind: calls whose GPU
  *   work overlaps (two streams, two host threads) race and corrupt each
  *   other's results, so serialize them.  Synchronizes `stream`.
@@ -193,8 +193,14 @@ GPTQ_API size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const
  *     128-column lazy batches ([G] §2.2; after each block,
  *     W[:, i2:] -= Err U[i1:i2, i2:]).  At the first column of each group the
  *     group's scale and zero point are set from the group's current,
- *     error-updated values.  Codes are decided in fp32:
- *     code = clamp(rint(w * (1/s)) + z, 0, 2^bits - 1).
+ *     error-updated values: span = max - min over the group's range
+ *     (asymmetric; the range always includes 0) or 2 max|w| (symmetric),
+ *     s = span / maxq, and
+ *     code = clamp(rint(w / s) + z, 0, maxq), maxq = 2^bits - 1,
+ *     round half to even, with w / s taken as maxq * (w / span) and w / span
+ *     rounded as IEEE fp32 division rounds it (so a weight exactly halfway
+ *     between two levels, like -max|w| on the symmetric grid, is decided as
+ *     a tie).
  *   W       [d_row, d_col] of type w_dtype (GPTQ_W_FP32/BF16/FP16), 16-byte
  *           aligned.  Read only (the fp32 working copy lives in ws).
  *   U, perm outputs of gptq_prepare_hinv for the same cfg.

@@ -16,13 +16,13 @@ Sources (the web pages this method is described on):
   [S]  "AWQ与GPTQ谁更强？ms-swift量化模块深度评测", GPTQ section
        (GptqConfig(..., damp_percent=0.01, desc_act, sym=True)).
 
-Precision: the numeric state (H, U, W during the column loop, errors) is
-fp64.  Where floating point decides an integer -- the zero point and each
-quantized code -- the decision is taken in IEEE fp32 with exactly the
-formula the CUDA kernels use, so that both sides decide in the same
-precision: r = fl32(1/s), code = clamp(rint(fl32(w32 * r)) + z, 0, maxq),
-z = rint(fl32(-xmin32 * r)), with s = fl32(fl32(xmax32 - xmin32) / maxq).
-The scale s is therefore an fp32 number on both sides.
+Precision: everything is fp64 -- H, U, the weights during the column loop,
+the errors, and the quantizer decisions.  The one fp32 number is the
+group's scale: it is stored as fp32 (the output type of the scales), and the
+zero point and every code are decided against that stored value with the
+plain definitions, z = rint(-xmin / s) and code = clamp(rint(w / s) + z, 0,
+maxq), so that the grid the codes were chosen on is the grid s * (q - z)
+that dequantization rebuilds.
 
 Readings taken where the pages are silent or garbled (each listed in the
 design notes):
@@ -41,7 +41,8 @@ design notes):
      a valid unsigned code.
   R7 (symmetric): a = max(|xmin|, xmax), s = 2a/maxq, z = (maxq+1)/2.
   R8 (degenerate range xmin == xmax): use [-1, +1].
-  R9 (rounding): round half to even.
+  R9 (rounding): round half to even, applied to the exact quotient w / s
+     (here evaluated in fp64).
   R10 (groups under desc_act): gs consecutive columns in processing order;
       g_idx maps each original column to its group.
   R11 (packing, not on the pages): LSB-first along the input dimension;
@@ -210,42 +211,51 @@ def maxq_of(bits: int) -> int:
 
 
 def quant_params(w: np.ndarray, bits: int, sym: bool, include_zero: bool = True):
-    """Scale and zero point per row of w [rows, g] (R6-R8), decided in fp32.
+    """Grid of each row of w [rows, g] (R6-R8), from the fp64 values.
 
-    Returns (scale float32 [rows], zero int64 [rows]).  include_zero=False
-    gives the unconstrained min-max grid of the pages' worked example (the
-    zero point may then fall outside [0, maxq]); the solver always uses
-    include_zero=True.
+    Asymmetric: xmin = min(0, min w), xmax = max(0, max w) (R6), span =
+    xmax - xmin, s = span / maxq, z = rint(-xmin / s).  Symmetric (R7):
+    a = max(|xmin|, xmax), span = 2a, s = 2a / maxq, z = (maxq + 1) / 2.  An
+    empty range (xmin == xmax, or a == 0) uses [-1, 1] instead (R8).
+
+    Returns (scale float32 [rows], zero int64 [rows], span float64 [rows]).
+    The scale is stored as fp32, the output type; decisions (the zero point
+    here, the codes in quantize_codes) are taken on the exact quotient
+    x / s = maxq * (x / span), not on the stored fp32 scale (R9).
+    include_zero=False gives the unconstrained min-max grid of the pages'
+    worked example (the zero point may then fall outside [0, maxq]); the
+    solver always uses include_zero=True.
     """
-    maxq = np.float32(maxq_of(bits))
-    w32 = np.asarray(w, dtype=np.float64).astype(np.float32)
-    xmin = w32.min(axis=1)
-    xmax = w32.max(axis=1)
+    maxq = maxq_of(bits)
+    w64 = np.asarray(w, dtype=np.float64)
+    xmin = w64.min(axis=1)
+    xmax = w64.max(axis=1)
     if include_zero:
-        xmin = np.minimum(xmin, np.float32(0.0))
-        xmax = np.maximum(xmax, np.float32(0.0))
+        xmin = np.minimum(xmin, 0.0)
+        xmax = np.maximum(xmax, 0.0)
     if sym:
         a = np.maximum(np.abs(xmin), xmax)
-        a = np.where(a == 0, np.float32(1.0), a).astype(np.float32)
-        scale = (np.float32(2.0) * a) / maxq
-        zero = np.full(w32.shape[0], (maxq_of(bits) + 1) // 2, dtype=np.int64)
-        return scale.astype(np.float32), zero
-    deg = xmin == xmax
-    xmin = np.where(deg, np.float32(-1.0), xmin).astype(np.float32)
-    xmax = np.where(deg, np.float32(1.0), xmax).astype(np.float32)
-    scale = ((xmax - xmin).astype(np.float32) / maxq).astype(np.float32)
-    rcp = (np.float32(1.0) / scale).astype(np.float32)
-    zero = np.rint((-xmin * rcp).astype(np.float32)).astype(np.int64)
-    return scale, zero
+        a = np.where(a == 0, 1.0, a)
+        span = 2.0 * a
+        zero = np.full(w64.shape[0], (maxq + 1) // 2, dtype=np.int64)
+    else:
+        deg = xmin == xmax
+        xmin = np.where(deg, -1.0, xmin)
+        xmax = np.where(deg, 1.0, xmax)
+        span = xmax - xmin
+        zero = np.rint(maxq * (-xmin / span)).astype(np.int64)
+    scale = (span / maxq).astype(np.float32)
+    return scale, zero, span
 
 
-def quantize_codes(w: np.ndarray, scale: np.ndarray, zero: np.ndarray, bits: int) -> np.ndarray:
-    """code = clamp(rint(w/s) + z, 0, maxq), decided in fp32 as
-    rint(fl32(w32 * fl32(1/s))) (R9)."""
-    w32 = np.asarray(w, dtype=np.float64).astype(np.float32)
-    rcp = (np.float32(1.0) / np.asarray(scale, dtype=np.float32)).astype(np.float32)
-    t = np.rint((w32 * rcp).astype(np.float32)).astype(np.int64)
-    return np.clip(t + zero, 0, maxq_of(bits))
+def quantize_codes(w: np.ndarray, span: np.ndarray, zero: np.ndarray, bits: int) -> np.ndarray:
+    """code = clamp(rint(w / s) + z, 0, maxq) with s = span / maxq (R9),
+    evaluated in fp64 as rint(maxq * (w / span)), half to even.  Written this
+    way, a weight exactly at a grid midpoint (such as -a on the symmetric
+    grid, which lands on -maxq/2) gives an exact midpoint here too."""
+    maxq = maxq_of(bits)
+    t = np.rint(maxq * (np.asarray(w, dtype=np.float64) / np.asarray(span, dtype=np.float64)))
+    return np.clip(t.astype(np.int64) + zero, 0, maxq)
 
 
 def dequantize_codes(q: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.ndarray:
@@ -314,20 +324,20 @@ def column_loop(Wp: np.ndarray, U: np.ndarray, cfg, *, blocksize: int | None = N
     zeros = np.zeros((n_groups, rows), dtype=np.int64)
     codes = np.zeros((rows, d_col), dtype=np.int64)
     Q = np.zeros((rows, d_col), dtype=np.float64)
+    spans = np.zeros((n_groups, rows), dtype=np.float64)
     if gs == -1:
-        scales[0], zeros[0] = quant_params(W, cfg.bits, cfg.sym)
-    s = scales[0].copy()
-    z = zeros[0].copy()
+        scales[0], zeros[0], spans[0] = quant_params(W, cfg.bits, cfg.sym)
+    s, z, sp = scales[0].copy(), zeros[0].copy(), spans[0].copy()
     for i1 in range(0, d_col, B):
         i2 = min(i1 + B, d_col)
         Err = np.zeros((rows, i2 - i1), dtype=np.float64)
         for j in range(i1, i2):
             if gs != -1 and j % gs == 0:
                 g = j // gs
-                scales[g], zeros[g] = quant_params(W[:, j:j + gs], cfg.bits, cfg.sym)
-                s, z = scales[g].copy(), zeros[g].copy()
+                scales[g], zeros[g], spans[g] = quant_params(W[:, j:j + gs], cfg.bits, cfg.sym)
+                s, z, sp = scales[g].copy(), zeros[g].copy(), spans[g].copy()
             w = W[:, j]
-            q = quantize_codes(w, s, z, cfg.bits)
+            q = quantize_codes(w, sp, z, cfg.bits)
             dq = dequantize_codes(q, s, z)
             e = obq_error(w, dq, U[j, j])
             obq_update(W, e, U, j, j + 1, i2)
@@ -403,8 +413,8 @@ def rtn(W: np.ndarray, cfg) -> LayerResult:
     Q = np.zeros((d_row, d_col))
     for g in range(n_groups):
         blk = W64[:, g * width:(g + 1) * width]
-        scales[g], zeros[g] = quant_params(blk, cfg.bits, cfg.sym)
-        q = quantize_codes(blk, scales[g][:, None], zeros[g][:, None], cfg.bits)
+        scales[g], zeros[g], span = quant_params(blk, cfg.bits, cfg.sym)
+        q = quantize_codes(blk, span[:, None], zeros[g][:, None], cfg.bits)
         codes[:, g * width:(g + 1) * width] = q
         Q[:, g * width:(g + 1) * width] = dequantize_codes(q, scales[g][:, None],
                                                           zeros[g][:, None])

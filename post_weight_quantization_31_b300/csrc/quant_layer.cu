@@ -32,12 +32,15 @@
 //              traffic on W).  A = Err (hi/lo, written by the column
 //              kernel), B = U^T rows (hi/lo, split once per call)
 //
-// Code decisions are taken in fp32 exactly as:
-//   s = (xmax - xmin) / maxq,  r = 1 / s,  z = rint(-xmin * r)   (asym)
-//   s = 2 a / maxq, r = 1 / s, z = (maxq + 1) / 2, a = max(-xmin, xmax) (sym)
-//   code = min(max(rint(w * r) + z, 0), maxq)
-// with xmin = min(0, min w), xmax = max(0, max w), and the range [-1, 1]
-// when it is empty.
+// The grid of a group (fp32 working values):
+//   asym: xmin = min(0, min w), xmax = max(0, max w), span = xmax - xmin
+//   sym:  a = max(-xmin, xmax), span = 2a;  an empty range uses [-1, 1]
+//   s = span / maxq (stored), z = rint(-xmin / s) (asym) or (maxq + 1)/2
+//   code = clamp(rint(w / s) + z, 0, maxq), round half to even.
+// Every quotient w / s is taken as maxq * (w / span), with w / span
+// rounded as IEEE division rounds it, so that a weight exactly at a grid
+// midpoint (the symmetric grid puts -a at -maxq/2) stays exactly there and
+// half-to-even decides it, whatever way the stored scale was rounded.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -57,29 +60,50 @@ constexpr int CL_THREADS = 256;
 constexpr int CL_ROWS = CL_THREADS / LPR;
 
 struct QParams {
-  float s, r, z;
+  float s;     // stored scale, span / maxq
+  float span;  // xmax - xmin, or 2a
+  float rsp;   // 1 / span (IEEE-rounded)
+  float z;     // zero point
 };
+
+// x / span as IEEE division rounds it: q0 = x * RN(1/span), then one
+// correction by the residual x - span * q0, which a fused multiply-add gives
+// exactly.  With a correctly rounded reciprocal this one step yields the
+// correctly rounded quotient (Markstein's division theorem); a GPU test
+// checks it bit for bit against CUDA's IEEE division.
+__device__ __forceinline__ float div_span(float x, const QParams& p) {
+  const float q0 = x * p.rsp;
+  const float res = fmaf(-q0, p.span, x);
+  return fmaf(res, p.rsp, q0);
+}
+
+__device__ __forceinline__ QParams grid_from_span(float span, float neg_xmin, float maxq, int sym) {
+  QParams p;
+  p.span = span;
+  p.s = span / maxq;
+  p.rsp = 1.f / span;
+  p.z = sym ? 0.5f * (maxq + 1.f) : rintf(maxq * div_span(neg_xmin, p));
+  return p;
+}
 
 __device__ __forceinline__ QParams grid_params(float xmin, float xmax, float maxq, int sym) {
   xmin = fminf(xmin, 0.f);
   xmax = fmaxf(xmax, 0.f);
-  QParams p;
   if (sym) {
     float a = fmaxf(-xmin, xmax);
     if (a == 0.f) a = 1.f;
-    p.s = (2.f * a) / maxq;
-    p.r = 1.f / p.s;
-    p.z = 0.5f * (maxq + 1.f);
-  } else {
-    if (xmin == xmax) {
-      xmin = -1.f;
-      xmax = 1.f;
-    }
-    p.s = (xmax - xmin) / maxq;
-    p.r = 1.f / p.s;
-    p.z = rintf(-xmin * p.r);
+    return grid_from_span(2.f * a, a, maxq, 1);
   }
-  return p;
+  if (xmin == xmax) {
+    xmin = -1.f;
+    xmax = 1.f;
+  }
+  return grid_from_span(xmax - xmin, -xmin, maxq, 0);
+}
+
+// clamp(rint(w / s) + z, 0, maxq) as a float.
+__device__ __forceinline__ float grid_code(float w, const QParams& p, float maxq) {
+  return fminf(fmaxf(rintf(maxq * div_span(w, p)) + p.z, 0.f), maxq);
 }
 
 template <typename T>
@@ -117,7 +141,8 @@ __global__ void load_w_kernel(const T* __restrict__ W, const int32_t* __restrict
 
 // group_size = -1: (scale, zero) per row from the initial row.
 __global__ void row_params_kernel(const float* __restrict__ Wf, int d_col, float maxq, int sym,
-                                  float* __restrict__ scales, uint8_t* __restrict__ zeros) {
+                                  float* __restrict__ scales, uint8_t* __restrict__ zeros,
+                                  float* __restrict__ spans) {
   __shared__ float smn[32], smx[32];
   const int r = blockIdx.x;
   const float* w = Wf + static_cast<size_t>(r) * d_col;
@@ -143,6 +168,7 @@ __global__ void row_params_kernel(const float* __restrict__ Wf, int d_col, float
     const QParams p = grid_params(mn, mx, maxq, sym);
     scales[r] = p.s;
     zeros[r] = static_cast<uint8_t>(p.z);
+    spans[r] = p.span;
   }
 }
 
@@ -160,6 +186,7 @@ struct ColumnArgs {
   float* Err_hi;        // [d_row, SB] scaled errors of the super-block, TF32 split;
   float* Err_lo;        // this block writes columns [err_col0, err_col0 + ncols)
   int err_col0;
+  const float* row_span;  // group_size = -1: span of each row's grid
 };
 
 __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) {
@@ -208,10 +235,11 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
     w[k + 2] = v.z;
     w[k + 3] = v.w;
   }
-  QParams p{1.f, 1.f, 0.f};
+  QParams p{1.f, 1.f, 1.f, 0.f};
   if (a.gs <= 0 && row_ok) {
     p.s = a.scales[r];
-    p.r = 1.f / p.s;
+    p.span = a.row_span[r];
+    p.rsp = 1.f / p.span;
     p.z = static_cast<float>(a.zeros[r]);
   }
   __syncthreads();
@@ -250,7 +278,7 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
       }
       const int j = CPL * seg + k;
       const float v = __shfl_sync(0xffffffffu, w[k], src_base | seg);
-      const float q = fminf(fmaxf(rintf(v * p.r) + p.z, 0.f), a.maxq);
+      const float q = grid_code(v, p, a.maxq);
       const float dq = p.s * (q - p.z);
       const float e = (v - dq) * inv_d[j];
       const float* urow = urow_base + k * UROW;
@@ -317,7 +345,7 @@ constexpr size_t kColumnSmem =
     sizeof(float) * (CB * UROW + CB + CL_ROWS * (CB + 1)) + CL_ROWS * CB;
 
 struct QuantLayout {
-  size_t status, Wf, Err_hi, Err_lo, Ut_hi, Ut_lo, total;
+  size_t status, row_span, Wf, Err_hi, Err_lo, Ut_hi, Ut_lo, total;
 };
 
 static size_t align256q(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -327,6 +355,8 @@ static QuantLayout quant_layout(int64_t d_row, int64_t d_col) {
   size_t off = 0;
   L.status = off;
   off += 256;
+  L.row_span = off;
+  off = align256q(off + sizeof(float) * d_row);
   L.Wf = off;
   off = align256q(off + sizeof(float) * d_row * d_col);
   L.Err_hi = off;
@@ -351,6 +381,7 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
   const QuantLayout L = quant_layout(d_row64, d_col64);
   char* base = static_cast<char*>(ws);
   int* status = reinterpret_cast<int*>(base + L.status);
+  float* row_span = reinterpret_cast<float*>(base + L.row_span);
   float* Wf = reinterpret_cast<float*>(base + L.Wf);
   float* Err_hi = reinterpret_cast<float*>(base + L.Err_hi);
   float* Err_lo = reinterpret_cast<float*>(base + L.Err_lo);
@@ -374,7 +405,7 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
     GPTQ_LAUNCH_CHECK();
   }
   if (gs <= 0) {
-    row_params_kernel<<<d_row, 256, 0, st>>>(Wf, d_col, maxq, cfg.sym, scales, zeros);
+    row_params_kernel<<<d_row, 256, 0, st>>>(Wf, d_col, maxq, cfg.sym, scales, zeros, row_span);
     GPTQ_LAUNCH_CHECK();
   }
   {
@@ -428,6 +459,7 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
       ca.Err_hi = Err_hi;
       ca.Err_lo = Err_lo;
       ca.err_col0 = i1 - sb0;
+      ca.row_span = row_span;
       GPTQ_CUDA_TRY(launch_pdl(column_block_kernel, dim3((d_row + CL_ROWS - 1) / CL_ROWS),
                                dim3(CL_THREADS), kColumnSmem, st, ca));
       GPTQ_LAUNCH_CHECK();
@@ -447,3 +479,28 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
 }
 
 }  // namespace gptq
+
+namespace {
+__global__ void div_span_probe_kernel(const float* __restrict__ x, const float* __restrict__ span,
+                                      int n, float* __restrict__ q_grid,
+                                      float* __restrict__ q_ieee) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  gptq::QParams p;
+  p.span = span[i];
+  p.rsp = 1.f / p.span;
+  q_grid[i] = gptq::div_span(x[i], p);
+  q_ieee[i] = __fdiv_rn(x[i], span[i]);
+}
+}  // namespace
+
+// Test hook (not part of the public header): the grid's quotient x / span
+// next to CUDA's IEEE division of the same operands, for n pairs.
+extern "C" GPTQ_API int gptq_internal_div_span(const float* x, const float* span, int n,
+                                               float* q_grid, float* q_ieee, gptq_stream_t stream) {
+  if (n <= 0) return GPTQ_OK;
+  div_span_probe_kernel<<<(n + 255) / 256, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      x, span, n, q_grid, q_ieee);
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
+}

@@ -64,3 +64,34 @@ def test_tgemm_3xtf32(lib, M, N, K, lower, row_off):
     scale = np.abs(A).astype(np.float64) @ np.abs(B).astype(np.float64).T + np.abs(C0)
     err = np.max(np.abs(got - want) / scale)
     assert err < 2e-6, err
+
+
+def test_grid_quotient_equals_ieee_division(lib):
+    """The column loop decides codes on maxq * (w / span) with w / span taken
+    from the reciprocal plus one exact-residual correction; it must equal
+    CUDA's IEEE division bit for bit, on random operands and on the exact
+    midpoints of the symmetric grid (w = -span/2)."""
+    import torch
+    f = lib.gptq_internal_div_span
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    rng = np.random.Generator(np.random.PCG64(99))
+    n = 1 << 20
+    span = rng.uniform(1e-4, 0.5, n).astype(np.float32)
+    x = (rng.standard_normal(n) * 0.05).astype(np.float32)
+    k = n // 8
+    x[:k] = -0.5 * span[:k]                        # exact midpoints
+    x[k:2 * k] = span[k:2 * k]                     # quotient exactly 1
+    span[2 * k:3 * k] = np.float32(2.0) ** rng.integers(-12, 0, k).astype(np.float32)
+    tx, ts = torch.from_numpy(x).cuda(), torch.from_numpy(span).cuda()
+    qg, qi = torch.empty_like(tx), torch.empty_like(tx)
+    assert f(tx.data_ptr(), ts.data_ptr(), n, qg.data_ptr(), qi.data_ptr(),
+             torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    a, b = qg.cpu().numpy(), qi.cpu().numpy()
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert np.all(a[:k] == -0.5) and np.all(a[k:2 * k] == 1.0)
+    # and IEEE division itself: the fp64 quotient rounded once to fp32
+    want = (x.astype(np.float64) / span.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(b, want)

@@ -147,15 +147,29 @@ def test_correlated_inputs_quality():
 
 def test_identity_hessian_gives_rtn():
     """P1 on the GPU: X with orthogonal rows of equal norm makes H a multiple
-    of I, so the GPU must reproduce round-to-nearest exactly."""
+    of I, so the GPU must reproduce round-to-nearest exactly.  The weights
+    are bf16 values and stay unchanged (no compensation), so both sides
+    decide on the same numbers; the test first checks that no quotient
+    maxq * w / span lies so near a rounding midpoint that fp32 and fp64
+    could legitimately disagree (exact midpoints, like the symmetric grid's
+    -a, are decided the same way by both)."""
     import torch
     from post_weight_quantization_31_b300 import api
     d_col, d_row = 256, 64
     X = np.zeros((d_col, 512), dtype=np.float16)
     X[np.arange(d_col), np.arange(d_col)] = 1.0
     W = wl.make_weight(d_row, d_col, seed=3, dtype="bf16")
-    for kw in (dict(), dict(sym=True, bits=3, group_size=32), dict(group_size=-1, bits=2)):
+    for kw in (dict(), dict(sym=True), dict(sym=True, bits=3, group_size=32),
+               dict(group_size=-1, bits=2), dict(bits=8, group_size=32)):
         cfg = qc(**kw)
+        gs = d_col if cfg.group_size == -1 else cfg.group_size
+        maxq = (1 << cfg.bits) - 1
+        for g0 in range(0, d_col, gs):
+            blk = W[:, g0:g0 + gs].astype(np.float64)
+            _s, _z, span = O.quant_params(blk, cfg.bits, cfg.sym)
+            t = maxq * blk / span[:, None]
+            frac = np.abs(t - np.floor(t) - 0.5)
+            assert np.all((frac == 0) | (frac > 1e-5)), kw
         g = P.gpu_solve(W, "bf16", X, cfg)
         r = O.rtn(W, cfg)
         assert np.array_equal(g.codes, r.codes), kw

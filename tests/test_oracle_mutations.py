@@ -9,6 +9,7 @@ import pytest
 import oracle as O
 import oracle.gptq_oracle as G
 from post_weight_quantization_31_b300 import workloads as wl
+from tests.test_oracle_golden import check_grid_examples
 from tests.test_oracle_pins import _ls_check
 
 
@@ -20,9 +21,9 @@ def cfg(**kw):
 
 
 def pins_hold():
-    """A compact run of P1, P2, P3, P4, I1, I2 and the nearest-level pin;
-    returns the names of the pins that fail."""
-    failed = []
+    """A compact run of P1, P2, P3, P4, I1, the nearest-level pin and the
+    hand-worked quantizer grids; returns the names of the pins that fail."""
+    failed = ["grid: " + name for name in check_grid_examples()]
     # P1
     W = wl.make_weight(8, 64, seed=1, dtype="bf16")
     c = cfg()
@@ -57,8 +58,8 @@ def pins_hold():
     # nearest level: every in-range weight lands on its nearest grid point
     rng = np.random.Generator(np.random.PCG64(6))
     w = rng.standard_normal((50, 16))
-    s, z = G.quant_params(w, 4, False)
-    q = G.quantize_codes(w, s[:, None], z[:, None], 4)
+    s, z, span = G.quant_params(w, 4, False)
+    q = G.quantize_codes(w, span[:, None], z[:, None], 4)
     dq = G.dequantize_codes(q, s[:, None], z[:, None])
     grid = s[:, None, None].astype(np.float64) * (np.arange(16)[None, None, :] - z[:, None, None])
     nearest = np.min(np.abs(w[:, :, None] - grid), axis=2)
@@ -85,16 +86,67 @@ MUTATIONS = {
     "damp_from_S": ("damped_hessian",
                     lambda S, n, d: (2.0 / n) * S + d * np.mean(np.diag(S)) * np.eye(S.shape[0])),
     "floor_rounding": ("quantize_codes",
-                       lambda w, s, z, bits: np.clip(np.floor(
-                           (np.asarray(w, np.float64).astype(np.float32)
-                            * (np.float32(1) / np.asarray(s, np.float32))).astype(np.float32)
+                       lambda w, span, z, bits: np.clip(np.floor(
+                           ((1 << bits) - 1) * (np.asarray(w, np.float64) / span)
                        ).astype(np.int64) + z, 0, (1 << bits) - 1)),
     "hinv_not_factored": ("hinv_upper", lambda H: np.triu(np.linalg.inv(H))),
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def _mutant_quant_params(mistake: str):
+    """The quantizer grid with one planted mistake (R6-R8 otherwise)."""
+    def quant_params(w, bits, sym, include_zero=True):
+        maxq = (1 << bits) - 1
+        w64 = np.asarray(w, dtype=np.float64)
+        xmin, xmax = w64.min(axis=1), w64.max(axis=1)
+        if include_zero and mistake != "zero_clamp_dropped":
+            xmin, xmax = np.minimum(xmin, 0.0), np.maximum(xmax, 0.0)
+        with np.errstate(all="ignore"):
+            if sym:
+                a = np.maximum(np.abs(xmin), np.abs(xmax))
+                if mistake != "empty_range_kept":
+                    a = np.where(a == 0, 1.0, a)
+                span = a if mistake == "sym_scale_a_over_maxq" else 2.0 * a
+                zero = np.full(w64.shape[0], maxq // 2 if mistake == "sym_zero_maxq_half"
+                               else (maxq + 1) // 2, dtype=np.int64)
+            else:
+                if mistake != "empty_range_kept":
+                    deg = xmin == xmax
+                    xmin, xmax = np.where(deg, -1.0, xmin), np.where(deg, 1.0, xmax)
+                span = xmax - xmin
+                zero = np.nan_to_num(np.rint(maxq * (-xmin / span))).astype(np.int64)
+            return (span / maxq).astype(np.float32), zero, span
+    return quant_params
+
+
+def _mutant_codes(w, span, z, bits):
+    with np.errstate(all="ignore"):
+        t = np.nan_to_num(np.rint(((1 << bits) - 1) * (np.asarray(w, np.float64) / span)))
+    return np.clip(t.astype(np.int64) + z, 0, (1 << bits) - 1)
+
+
+def test_grid_mutant_without_a_mistake_passes(monkeypatch):
+    """Control: the mutant grid with no mistake planted passes every pin, so
+    a failure below comes from the planted mistake alone."""
+    monkeypatch.setattr(G, "quant_params", _mutant_quant_params("none"))
+    monkeypatch.setattr(G, "quantize_codes", _mutant_codes)
+    assert pins_hold() == []
+
+
+GRID_MUTATIONS = ("sym_scale_a_over_maxq", "sym_zero_maxq_half", "zero_clamp_dropped",
+                  "empty_range_kept")
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS) + list(GRID_MUTATIONS))
 def test_planted_mistake_is_caught(name, monkeypatch):
-    attr, fn = MUTATIONS[name]
-    monkeypatch.setattr(G, attr, fn)
-    assert pins_hold() != [], name
+    if name in GRID_MUTATIONS:
+        monkeypatch.setattr(G, "quant_params", _mutant_quant_params(name))
+        monkeypatch.setattr(G, "quantize_codes", _mutant_codes)
+    else:
+        attr, fn = MUTATIONS[name]
+        monkeypatch.setattr(G, attr, fn)
+    failed = pins_hold()
+    assert failed != [], name
+    if name in GRID_MUTATIONS:
+        # the hand-worked grids are the pins that catch a wrong grid
+        assert any(f.startswith("grid: ") for f in failed), (name, failed)

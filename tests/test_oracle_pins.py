@@ -166,12 +166,12 @@ def test_i2_two_column_closed_form():
         c = cfg(bits=3, group_size=-1, blocksize=1)
         U = O.hinv_upper(H)
         codes, scales, zeros, Q = O.column_loop(w, U, c, blocksize=1)
-        s, z = O.quant_params(w, 3, False)
-        q0 = O.quantize_codes(w[:, 0], s, z, 3)
+        s, z, span = O.quant_params(w, 3, False)
+        q0 = O.quantize_codes(w[:, 0], span, z, 3)
         dq0 = s.astype(np.float64) * (q0 - z)
         w1 = w[:, 1] + (w[:, 0] - dq0) * H[0, 1] / H[1, 1]
         assert np.array_equal(codes[:, 0], q0)
-        assert np.array_equal(codes[:, 1], O.quantize_codes(w1, s, z, 3))
+        assert np.array_equal(codes[:, 1], O.quantize_codes(w1, span, z, 3))
 
 
 # ------------------------------------------------------------------ I3

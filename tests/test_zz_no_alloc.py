@@ -12,6 +12,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle as O
 from post_weight_quantization_31_b300 import _lib
 from post_weight_quantization_31_b300 import workloads as wl
 
@@ -61,8 +62,14 @@ def test_noalloc_matches_workspace_version_two_calls_in_a_row():
                                            stream)
         assert st == 0, _lib.status_name(st)
         torch.cuda.synchronize()
+        # The prepare step has no floating-point atomics: with the same inputs
+        # it is deterministic, so the fixed scratch array must give exactly the
+        # caller-workspace result, whatever the previous call left in it.
         assert np.array_equal(perm.cpu().numpy(), perm_ref.cpu().numpy())
-        Ug, Ur = U.cpu().numpy().astype(np.float64), U_ref.cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(Ug))
-        err = np.max(np.abs(Ug - Ur)) / np.max(np.abs(Ur))
+        Ug, Ur = U.cpu().numpy(), U_ref.cpu().numpy()
+        assert np.array_equal(Ug.view(np.uint32), Ur.view(np.uint32)), d_col
+        # and both agree with the oracle's factor of the same Hessian
+        perm_o, Hp, U_o = O.prepare(O.hessian_sum(X), n, cfg)
+        assert np.array_equal(perm.cpu().numpy(), perm_o)
+        err = np.max(np.abs(Ug.astype(np.float64) - U_o)) / np.max(np.abs(U_o))
         assert err < 2e-4, (d_col, err)
