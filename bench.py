@@ -278,6 +278,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         clk.mark("end")
+    solver.check()      # device-side status of the last prepare / quantize
     if dist is not None:
         dist.barrier()
     launches = api.launch_count() - n0
@@ -348,6 +349,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     }
     if args.dequant_reps > 0:
         line["dequant"] = measure_dequant(solver, cfg, stream, peaks, args.dequant_reps)
+    if args.layer_set_layers > 0:
+        del X, W, solver
+        torch.cuda.empty_cache()
+        line["layer_set"] = measure_layer_set(layer_set_inputs(dev), args.layer_set_layers, dev)
     if args.cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, quick=args.quick_cpu)
     if dist is not None:
@@ -425,24 +430,10 @@ def run_dequant_only(args) -> dict:
 LAYER_SET_SITES = ("qkv", "o", "gate_up", "down")
 
 
-def run_layer_set(args) -> dict:
-    """--layer-set L: the 7B-shaped layer set, L decoder layers x 4 input
-    sites (q|k|v rows stacked on one X, o, gate|up stacked, down; 4-bit sym
-    g128, 65536 tokens per site).  Each site: S = 0, accumulate, prepare,
-    quantize, pack.  The inputs of one decoder layer are generated once (the
-    seeded generators of workloads.py) and reused for every layer: each
-    layer does the same work on data of the same distribution.
-      sequential: one stream, layer after layer, site after site;
-      concurrent: the four sites of each layer on four streams (one host
-      thread each; the library's status reads block only their own stream).
-    Both are timed between CUDA events / device synchronizations."""
-    import threading
-
+def layer_set_inputs(dev) -> dict:
+    """One decoder layer's inputs of the 7B-shaped layer set, on the device."""
     import torch
-    from post_weight_quantization_31_b300 import api, build_lib, workloads as wl
-    build_lib.build()
-    dev = torch.device("cuda", 0)
-    L = int(args.layer_set)
+    from post_weight_quantization_31_b300 import api, workloads as wl
     sites = {}
     for site in LAYER_SET_SITES:
         inp = wl.decoder_site_7b(site, layer=0)
@@ -450,6 +441,21 @@ def run_layer_set(args) -> dict:
         sites[site] = dict(X=torch.from_numpy(inp.X).to(dev),
                            W=torch.from_numpy(inp.W).to(torch.bfloat16).to(dev),
                            solver=api.LayerSolver(d_row, d_col, inp.cfg, device=dev), weights=d_row * d_col)
+    return sites
+
+
+def measure_layer_set(sites: dict, L: int, dev) -> dict:
+    """L decoder layers x 4 input sites (q|k|v rows stacked on one X, o,
+    gate|up stacked, down; 4-bit sym g128, 65536 tokens per site).  Each
+    site: S = 0, accumulate, prepare, quantize, pack.  The inputs of one
+    decoder layer are reused for every layer: each layer does the same work
+    on data of the same distribution.
+      sequential: one stream, layer after layer, site after site;
+      concurrent: the four sites of each layer on four streams, enqueued
+      round-robin from one host thread (every library call is asynchronous).
+    Both are timed with CUDA events around the whole set; the device status
+    of every solve is checked afterwards."""
+    import torch
     weights_per_layer = sum(v["weights"] for v in sites.values())
 
     def solve(site):
@@ -460,51 +466,60 @@ def run_layer_set(args) -> dict:
         v["solver"].quantize(v["W"])
         v["solver"].pack()
 
+    main = torch.cuda.current_stream(dev)
     for site in LAYER_SET_SITES:          # warm-up
         solve(site)
     torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
     for _ in range(L):
         for site in LAYER_SET_SITES:
             solve(site)
+    e1.record(main)
     torch.cuda.synchronize(dev)
-    t_seq = time.perf_counter() - t0
+    t_seq = e0.elapsed_time(e1) * 1e-3
 
     streams = {site: torch.cuda.Stream(dev) for site in LAYER_SET_SITES}
-    errors = []
-
-    def worker(site):
-        try:
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    c0.record(main)
+    for st in streams.values():
+        st.wait_event(c0)
+    for _ in range(L):
+        for site in LAYER_SET_SITES:
             with torch.cuda.stream(streams[site]):
-                for _ in range(L):
-                    solve(site)
-            streams[site].synchronize()
-        except Exception as e:  # reported below; the other threads finish their layers
-            errors.append(f"{site}: {e}")
-
-    threads = [threading.Thread(target=worker, args=(site,)) for site in LAYER_SET_SITES]
+                solve(site)
+    for st in streams.values():
+        ev = torch.cuda.Event()
+        ev.record(st)
+        main.wait_event(ev)
+    c1.record(main)
     torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for th in threads:
-        th.start()
-    for th in threads:
-        th.join()
-    torch.cuda.synchronize(dev)
-    t_con = time.perf_counter() - t0
-    if errors:
-        raise RuntimeError("; ".join(errors))
-    return {"metric": "7B-shaped layer set: seconds per 32 decoder layers", "value": round(t_seq * 32 / L, 3),
-            "unit": "s", "n_gpus": 1, "higher_is_better": False, "data": "synthetic",
-            "config": {"workload": "32 x {q|k|v 12288x4096, o 4096x4096, gate|up 22016x4096, down 4096x11008} "
-                                   "bf16 N(0,0.02^2); X fp16 65536 tokens per site, N(0,1), 1% channels "
-                                   "x U[10,50]; 4-bit sym g128, damp 0.01, desc_act off",
-                       "layers_timed": L, "inputs": "one decoder layer's inputs, reused for every layer"},
-            "sequential_s": round(t_seq, 4), "concurrent_s": round(t_con, 4),
-            "sequential_s_per_32_layers": round(t_seq * 32 / L, 3),
-            "concurrent_s_per_32_layers": round(t_con * 32 / L, 3),
-            "weights_per_layer": int(weights_per_layer),
+    t_con = c0.elapsed_time(c1) * 1e-3
+    for site in LAYER_SET_SITES:
+        sites[site]["solver"].check()
+    return {"sequential_s_per_32_layers": round(t_seq * 32 / L, 4),
+            "concurrent_s_per_32_layers": round(t_con * 32 / L, 4),
+            "layers_timed": L, "weights_per_layer": int(weights_per_layer),
             "sequential_mweights_s": round(weights_per_layer * L / t_seq / 1e6, 1),
-            "concurrent_mweights_s": round(weights_per_layer * L / t_con / 1e6, 1)}
+            "concurrent_mweights_s": round(weights_per_layer * L / t_con / 1e6, 1),
+            "workload": "32 x {q|k|v 12288x4096, o 4096x4096, gate|up 22016x4096, down 4096x11008} "
+                        "bf16 N(0,0.02^2); X fp16 65536 tokens per site, N(0,1), 1% channels x "
+                        "U[10,50]; 4-bit sym g128, damp 0.01, desc_act off; one decoder layer's "
+                        "inputs reused for every layer"}
+
+
+def run_layer_set(args) -> dict:
+    """--layer-set L: the 7B-shaped layer set alone (see measure_layer_set)."""
+    import torch
+    from post_weight_quantization_31_b300 import build_lib
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    r = measure_layer_set(layer_set_inputs(dev), int(args.layer_set), dev)
+    return {"metric": "7B-shaped layer set: seconds per 32 decoder layers",
+            "value": r["sequential_s_per_32_layers"], "unit": "s", "n_gpus": 1,
+            "higher_is_better": False, "data": "synthetic",
+            "config": {"workload": r["workload"], "layers_timed": r["layers_timed"]}, **r}
 
 
 def run_sweep(args) -> dict:
@@ -545,6 +560,7 @@ def run_sweep(args) -> dict:
             step()
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        solver.check()
         ms = t0.elapsed_time(t1) / args.steps
         cases.append({"bits": bits, "group_size": gs, "desc_act": act, "ms_per_step": round(ms, 4),
                       "value": round(D * D / (ms * 1e-3) / 1e6, 3)})
@@ -726,6 +742,9 @@ def main() -> None:
                     help="time only the dequantization of a packed layer of this shape")
     ap.add_argument("--layer-set", default=None, metavar="L",
                     help="time L decoder layers of the 7B-shaped layer set (sequential and concurrent)")
+    ap.add_argument("--layer-set-layers", type=int, default=2,
+                    help="decoder layers of the 7B-shaped layer set timed after the main line "
+                         "(scaled to 32; 0: skip)")
     ap.add_argument("--sweep", default=None, metavar="BITS:GS[:act],...",
                     help="time the bench step for other quantizer settings")
     ap.add_argument("--dqgemm-only", default=None, metavar="MxNxK[,MxNxK...]",

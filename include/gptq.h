@@ -34,16 +34,29 @@
  *   - Matrices are row-major and densely packed unless a leading dimension
  *     is given.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
- *     stream).  gptq_prepare_hinv and gptq_quantize_layer synchronize the
- *     stream once at their end to read back a device status word; the other
- *     calls are asynchronous.
+ *     stream) and every call returns once it is enqueued, without waiting
+ *     for the GPU: the calls are stream-ordered and asynchronous, so the
+ *     solves of several layers can run concurrently on several streams.
+ *     Only gptq_workspace_status, gptq_device_fault and
+ *     gptq_prepare_hinv_noalloc wait for their stream.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and return GPTQ_ERR_INVALID_ARG (or GPTQ_ERR_WORKSPACE) with no side
  *     effect.  A CUDA error at launch returns GPTQ_ERR_CUDA.
+ *   - Errors found on the device (a non-positive pivot, non-finite input, a
+ *     wait that ran out) by gptq_prepare_hinv or gptq_quantize_layer are
+ *     recorded in a status word at the start of that call's workspace; read
+ *     it with gptq_workspace_status(ws, stream) after the call.  Each call
+ *     clears its own word when it starts, so the word describes the last
+ *     call that used the workspace, and a fault in one call never shows up
+ *     in another's.
  *   - Every wait inside a kernel is bounded in time (about 2 s).  A wait that
- *     runs out sets a sticky fault flag on the device and the kernel returns
- *     early; the next gptq_prepare_hinv / gptq_quantize_layer /
- *     gptq_device_fault call reports GPTQ_ERR_TIMEOUT and clears it.
+ *     runs out makes its kernel return early and records GPTQ_ERR_TIMEOUT:
+ *     in the call's workspace status word for gptq_prepare_hinv and
+ *     gptq_quantize_layer; for the calls without a workspace (hessian,
+ *     dequantize, dequant-matmul) in the library's per-device fault word,
+ *     which gptq_device_fault reads and clears.  That word is shared by all
+ *     streams of the device: a timeout there can stop, and is reported to,
+ *     whichever of those calls runs or checks next.
  *   - Only one device is used per call: the current device of the calling
  *     host thread.
  */
@@ -71,12 +84,17 @@ typedef struct CUstream_st* gptq_stream_t;
  * ([G] §3.3, [S]).
  *   bits          2, 3, 4 or 8.
  *   group_size    columns sharing one scale and zero point, counted in
- *                 processing order: a multiple of 32 that divides both
- *                 d_col and blocksize; or -1 for one group per row
- *                 ([E] FAQ Q6).
+ *                 processing order: 32, 64 or 128 (a divisor of d_col);
+ *                 or -1 for one group per row ([E] FAQ Q6).
  *   damp_percent  >= 0; lambda = damp_percent * mean(diag H) is added to
  *                 diag(H) ([G] §3.3, "防止矩阵奇异").
- *   blocksize     lazy-batch width ([G] §2.2); must be 128.
+ *   blocksize     lazy-batch width ([G] §2.2): any positive multiple of 32.
+ *                 Batching only changes the order in which the same
+ *                 compensation terms are summed (the result is the same in
+ *                 exact arithmetic), so the kernels keep their own two-level
+ *                 blocking -- 128-column blocks inside 512-column super-blocks
+ *                 -- and results agree with any blocksize up to fp32
+ *                 rounding.
  *   desc_act      0: natural column order; 1: descending diag(H), stable.
  *   sym           0: asymmetric grid over [min(0,min w), max(0,max w)];
  *                 1: symmetric grid, scale 2*max|w|/maxq, zero (maxq+1)/2.
@@ -152,8 +170,10 @@ GPTQ_API size_t gptq_prepare_workspace_size(int64_t d_col);
  *   perm    int32 [d_col] output: perm[i] = original column processed i-th.
  *   ws      workspace of at least gptq_prepare_workspace_size(d_col) bytes,
  *           256-byte aligned.
- *   Returns GPTQ_ERR_NOT_PD for a non-positive pivot (U is then undefined),
- *   GPTQ_ERR_NONFINITE for NaN/Inf in S.  Synchronizes `stream`.
+ *   Asynchronous.  Device-side errors land in the status word of ws
+ *   (gptq_workspace_status): GPTQ_ERR_NOT_PD for a non-positive pivot (U is
+ *   then undefined; retry with a larger damp_percent), GPTQ_ERR_NONFINITE
+ *   for NaN/Inf in S, GPTQ_ERR_TIMEOUT for a wait that ran out.
  */
 GPTQ_API gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
                                 const gptq_config_t* cfg, float* U, int32_t* perm,
@@ -210,8 +230,9 @@ GPTQ_API size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const
  *   zeros   uint8 [G, d_row] output.
  *   g_idx   int32 [d_col] output: group of each original column.
  *   ws      workspace of gptq_quantize_workspace_size bytes, 256-byte aligned.
- *   d_row % 32 == 0, d_col % 32 == 0.  Returns GPTQ_ERR_NONFINITE for NaN/Inf
- *   in W.  Synchronizes `stream`.
+ *   d_row % 32 == 0, d_col % 32 == 0.  Asynchronous: GPTQ_ERR_NONFINITE for
+ *   NaN/Inf in W and GPTQ_ERR_TIMEOUT land in the status word of ws
+ *   (gptq_workspace_status).
  */
 GPTQ_API gptq_status_t gptq_quantize_layer(const void* W, int32_t w_dtype, int64_t d_row,
                                   int64_t d_col, const float* U, const int32_t* perm,
@@ -298,9 +319,20 @@ GPTQ_API gptq_status_t gptq_dequant_matmul(const void* X, int32_t x_dtype, int64
 GPTQ_API const char* gptq_status_string(gptq_status_t status);
 
 /* Synchronizes `stream`; returns GPTQ_ERR_TIMEOUT (and clears the flag) if a
- * bounded wait ran out in any kernel of this library since the last check,
- * else GPTQ_OK (or GPTQ_ERR_CUDA). */
+ * bounded wait ran out since the last check in a kernel of a call that has
+ * no workspace (hessian, dequantize, dequant-matmul), else GPTQ_OK (or
+ * GPTQ_ERR_CUDA). */
 GPTQ_API gptq_status_t gptq_device_fault(gptq_stream_t stream);
+
+/*
+ * Waits for `stream` (cudaStreamSynchronize), then returns the status that
+ * the last gptq_prepare_hinv or gptq_quantize_layer call using the
+ * workspace `ws` (device pointer, the same one passed to that call) left in
+ * it: GPTQ_OK, GPTQ_ERR_NOT_PD, GPTQ_ERR_NONFINITE or GPTQ_ERR_TIMEOUT.
+ * `stream` must be the call's stream (or one ordered after it).  The word is
+ * left as it is; the next call on the workspace clears it when it starts.
+ */
+GPTQ_API gptq_status_t gptq_workspace_status(const void* ws, gptq_stream_t stream);
 
 /* Number of kernels this library has launched in this process (all
  * devices); for instrumentation. */

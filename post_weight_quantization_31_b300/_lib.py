@@ -53,6 +53,7 @@ SIGNATURES = {
                                    _vp, _vp]),
     "gptq_status_string": (ctypes.c_char_p, [_i32]),
     "gptq_device_fault": (_i32, [_vp]),
+    "gptq_workspace_status": (_i32, [_vp, _vp]),
     "gptq_launch_count": (ctypes.c_uint64, []),
 }
 

@@ -90,10 +90,21 @@ def prepare_workspace_size(d_col: int) -> int:
     return int(_lib.load().gptq_prepare_workspace_size(d_col))
 
 
+def workspace_status(ws: torch.Tensor, where: str = "gptq_workspace_status") -> None:
+    """Waits for the current stream and raises GPTQError if the last
+    prepare/quantize call on `ws` reported an error on the device."""
+    _check(_lib.load().gptq_workspace_status(ws.data_ptr(), _stream()), where)
+
+
 def prepare_hinv(S: torch.Tensor, n_seen: int, cfg: QuantConfig, diag: torch.Tensor | None = None,
                  U: torch.Tensor | None = None, perm: torch.Tensor | None = None,
-                 ws: torch.Tensor | None = None):
-    """Returns (U, perm): U fp32 [d, d] upper with H_perm^-1 = U^T U."""
+                 ws: torch.Tensor | None = None, check: bool = True):
+    """Returns (U, perm): U fp32 [d, d] upper with H_perm^-1 = U^T U.
+
+    The library call is asynchronous; with check=True (the default) this
+    waits for it and raises on a device-side error (NOT_PD, NONFINITE,
+    TIMEOUT).  With check=False the caller reads the status later with
+    workspace_status(ws)."""
     lib = _lib.load()
     d = S.shape[0]
     _need(S, torch.float32, "S", (d, d))
@@ -106,6 +117,8 @@ def prepare_hinv(S: torch.Tensor, n_seen: int, cfg: QuantConfig, diag: torch.Ten
     _check(lib.gptq_prepare_hinv(S.data_ptr(), _ptr(diag), d, int(n_seen), ctypes.byref(c),
                                  U.data_ptr(), perm.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _stream()), "gptq_prepare_hinv")
+    if check:
+        workspace_status(ws, "gptq_prepare_hinv")
     return U, perm
 
 
@@ -136,14 +149,19 @@ _WDT = {torch.float32: _lib.W_FP32, torch.bfloat16: _lib.W_BF16, torch.float16: 
 
 
 def quantize_layer(W: torch.Tensor, U: torch.Tensor, perm: torch.Tensor, cfg: QuantConfig,
-                   out: dict | None = None, ws: torch.Tensor | None = None) -> dict:
+                   out: dict | None = None, ws: torch.Tensor | None = None,
+                   check: bool = True) -> dict:
     """Returns dict(codes uint8 [d_row, d_col] original order, scales fp32
-    [G, d_row], zeros uint8 [G, d_row], g_idx int32 [d_col])."""
+    [G, d_row], zeros uint8 [G, d_row], g_idx int32 [d_col]).  `check` as
+    for prepare_hinv."""
     lib = _lib.load()
     if W.dtype not in _WDT:
         raise ValueError("W must be fp32, bf16 or fp16")
     _contig(W, "W")
     d_row, d_col = W.shape
+    _need(U, torch.float32, "U", (d_col, d_col))
+    _contig(U, "U")
+    _need(perm, torch.int32, "perm", (d_col,))
     dev = W.device
     G = n_groups(cfg.group_size, d_col)
     out = {} if out is None else out
@@ -158,6 +176,8 @@ def quantize_layer(W: torch.Tensor, U: torch.Tensor, perm: torch.Tensor, cfg: Qu
                                    perm.data_ptr(), ctypes.byref(c), codes.data_ptr(),
                                    scales.data_ptr(), zeros.data_ptr(), g_idx.data_ptr(),
                                    ws.data_ptr(), ws.numel(), _stream()), "gptq_quantize_layer")
+    if check:
+        workspace_status(ws, "gptq_quantize_layer")
     return out
 
 
@@ -295,11 +315,19 @@ class LayerSolver:
         self.n_seen += hessian_accumulate(X, self.S, self.diag)
 
     def prepare(self) -> None:
+        """Enqueues the prepare call (asynchronous; see check())."""
         prepare_hinv(self.S, self.n_seen, self.cfg, diag=self.diag, U=self.U, perm=self.perm,
-                     ws=self.ws_prep)
+                     ws=self.ws_prep, check=False)
 
     def quantize(self, W: torch.Tensor) -> None:
-        quantize_layer(W, self.U, self.perm, self.cfg, out=self.out, ws=self.ws_quant)
+        """Enqueues the quantize call (asynchronous; see check())."""
+        quantize_layer(W, self.U, self.perm, self.cfg, out=self.out, ws=self.ws_quant, check=False)
+
+    def check(self) -> None:
+        """Waits for the current stream and raises GPTQError if the last
+        prepare or quantize reported an error on the device."""
+        workspace_status(self.ws_prep, "gptq_prepare_hinv")
+        workspace_status(self.ws_quant, "gptq_quantize_layer")
 
     def pack(self) -> None:
         pack(self.out["codes"], self.out["zeros"], self.cfg.bits, self.cfg.group_size,
@@ -312,6 +340,7 @@ class LayerSolver:
         self.prepare()
         self.quantize(W)
         self.pack()
+        self.check()
         return self.result()
 
     def result(self) -> LayerResult:
@@ -374,6 +403,7 @@ def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
     solver.prepare()
     solver.quantize(W_dev)
     solver.pack()
+    solver.check()
     r = solver.result()
     return {"qweight": r.qweight.to("cpu"), "qzeros": r.qzeros.to("cpu"),
             "scales": r.scales.to("cpu"), "g_idx": r.g_idx.to("cpu")}

@@ -118,16 +118,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitLimitNs.  Returns false (after setting the sticky fault bit) if the
-// limit ran out or another thread of the grid already reported a fault.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* fault) {
+// limit_ns.  Returns false (after setting the timeout bit in *fault) if the
+// limit ran out, or if another wait that reports into the same word already
+// gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* fault,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*reinterpret_cast<volatile int*>(fault) & kStatTimeout) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(fault, kStatTimeout);
         return false;
       }

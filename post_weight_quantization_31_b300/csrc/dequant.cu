@@ -169,7 +169,8 @@ template <typename T, int BITS, bool STAGED>
 __global__ void __launch_bounds__(DQ_THREADS, 4) dequant_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w,
     const int32_t* __restrict__ qzeros, const float* __restrict__ scales,
-    const __grid_constant__ CUtensorMap tm_g, int d_row, int d_col, int n_groups, int* fault) {
+    const __grid_constant__ CUtensorMap tm_g, int d_row, int d_col, int n_groups, int* fault,
+    int stall, unsigned long long wait_ns) {
   extern __shared__ unsigned char dq_raw[];
   const uint32_t raw = smem_u32(dq_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -205,8 +206,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 4) dequant_kernel(
     int rb = static_cast<int>(t0 / n_chunks), ch = static_cast<int>(t0 % n_chunks);
     int s = 0;
     uint32_t ph = 0;                              // parity of the ring's current pass
-    for (long long t = t0; t < t1; ++t) {
-      if (issued >= DQ_STAGES && !mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1u, fault)) break;
+    // `stall` (a test launch only): issue no copy at all, so that every wait
+    // of the compute warps runs out while nothing is in flight.
+    for (long long t = t0; !stall && t < t1; ++t) {
+      if (issued >= DQ_STAGES && !mbar_wait_bounded(bar_empty + 8 * s, ph ^ 1u, fault, wait_ns)) break;
       mbar_arrive_expect_tx(bar_full + 8 * s, stage_bytes);
       const uint32_t dst = base + static_cast<uint32_t>(L.words + s * L.stage_bytes);
       tma_load_2d(dst, &tm_q, bar_full + 8 * s, rb * DQ_RB, ch * DQ_CHUNK * BITS / 32);
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 4) dequant_kernel(
     // Do not leave with copies in flight: wait (bounded) for the last loads.
     for (long long i = issued - DQ_STAGES < 0 ? 0 : issued - DQ_STAGES; i < issued; ++i)
       mbar_wait_bounded(bar_full + 8 * static_cast<int>(i % DQ_STAGES),
-                        static_cast<uint32_t>((i / DQ_STAGES) & 1), fault);
+                        static_cast<uint32_t>((i / DQ_STAGES) & 1), fault, wait_ns);
     return;
   }
 
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 4) dequant_kernel(
       }
     }
     int w_ok = 1;
-    if (lane == 0 && ok) w_ok = mbar_wait_bounded(bar_full + 8 * s, ph, fault);
+    if (lane == 0 && ok) w_ok = mbar_wait_bounded(bar_full + 8 * s, ph, fault, wait_ns);
     ok = ok && __shfl_sync(0xffffffffu, w_ok, 0);
     const int c0 = ch * DQ_CHUNK + warp * 32;     // this warp's first column
     const bool active = ok && c0 < d_col;         // d_col is a multiple of 32
@@ -318,7 +321,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 template <typename T, int BITS, bool STAGED>
 gptq_status_t launch_t(const CUtensorMap& tq, const CUtensorMap& tw, const CUtensorMap& tg,
                        const int32_t* qzeros, const float* scales, int d_row, int d_col, int n_groups,
-                       cudaStream_t st) {
+                       cudaStream_t st, int stall, unsigned long long wait_ns) {
   const DqLayout L(BITS, sizeof(T), n_groups, STAGED);
   auto kern = dequant_kernel<T, BITS, STAGED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total)) !=
@@ -332,7 +335,7 @@ gptq_status_t launch_t(const CUtensorMap& tq, const CUtensorMap& tw, const CUten
   const long long slots = static_cast<long long>(sm_count()) * per_sm;
   const unsigned grid = static_cast<unsigned>(tiles < slots ? tiles : slots);
   kern<<<grid, DQ_THREADS, L.total, st>>>(tq, tw, qzeros, scales, tg, d_row, d_col, n_groups,
-                                         fault_word_ptr());
+                                         fault_word_ptr(), stall, wait_ns);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
@@ -340,29 +343,30 @@ gptq_status_t launch_t(const CUtensorMap& tq, const CUtensorMap& tw, const CUten
 template <typename T, int BITS>
 gptq_status_t launch_bits(const CUtensorMap& tq, const CUtensorMap& tw, const CUtensorMap& tg,
                           const int32_t* qzeros, const float* scales, int d_row, int d_col, int n_groups,
-                          cudaStream_t st) {
+                          cudaStream_t st, int stall, unsigned long long wait_ns) {
   if (DqLayout(BITS, sizeof(T), n_groups, true).total <= DQ_SMEM_LIMIT)
-    return launch_t<T, BITS, true>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
-  return launch_t<T, BITS, false>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
+    return launch_t<T, BITS, true>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
+  return launch_t<T, BITS, false>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
 }
 
 template <typename T>
 gptq_status_t launch_dt(const CUtensorMap& tq, const CUtensorMap& tw, const CUtensorMap& tg,
                         const int32_t* qzeros, const float* scales, int d_row, int d_col, int bits,
-                        int n_groups, cudaStream_t st) {
+                        int n_groups, cudaStream_t st, int stall, unsigned long long wait_ns) {
   switch (bits) {
-    case 2: return launch_bits<T, 2>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
-    case 3: return launch_bits<T, 3>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
-    case 4: return launch_bits<T, 4>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
-    default: return launch_bits<T, 8>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st);
+    case 2: return launch_bits<T, 2>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
+    case 3: return launch_bits<T, 3>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
+    case 4: return launch_bits<T, 4>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
+    default: return launch_bits<T, 8>(tq, tw, tg, qzeros, scales, d_row, d_col, n_groups, st, stall, wait_ns);
   }
 }
 
 }  // namespace
 
-gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, const float* scales,
-                             const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits, int n_groups,
-                             int out_dtype, void* W, cudaStream_t st) {
+gptq_status_t launch_dequant_impl(const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                                  const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits,
+                                  int n_groups, int out_dtype, void* W, cudaStream_t st, int stall,
+                                  unsigned long long wait_ns) {
   auto fn = encode_fn();
   if (!fn || !fault_word_ptr()) return GPTQ_ERR_CUDA;
   const int out_bytes = out_dtype == GPTQ_W_FP32 ? 4 : 2;
@@ -403,10 +407,38 @@ gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, cons
       return GPTQ_ERR_INVALID_ARG;
   }
   const int r = static_cast<int>(d_row), c = static_cast<int>(d_col);
-  if (out_dtype == GPTQ_W_FP32) return launch_dt<float>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st);
+  if (out_dtype == GPTQ_W_FP32)
+    return launch_dt<float>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st, stall, wait_ns);
   if (out_dtype == GPTQ_W_BF16)
-    return launch_dt<__nv_bfloat16>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st);
-  return launch_dt<__half>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st);
+    return launch_dt<__nv_bfloat16>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st, stall, wait_ns);
+  return launch_dt<__half>(tq, tw, tg, qzeros, scales, r, c, bits, n_groups, st, stall, wait_ns);
+}
+
+gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, const float* scales,
+                             const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits, int n_groups,
+                             int out_dtype, void* W, cudaStream_t st) {
+  return launch_dequant_impl(qweight, qzeros, scales, g_idx, d_row, d_col, bits, n_groups, out_dtype, W,
+                             st, 0, kWaitLimitNs);
 }
 
 }  // namespace gptq
+
+// Test hook (not part of the public header): the dequantization kernel
+// launched with its producer stalled -- it issues no copy, so every bounded
+// wait of the compute warps runs out after wait_ns and the kernel returns
+// with GPTQ_ERR_TIMEOUT recorded in the library's fault word.  Nothing is in
+// flight when the waits give up; used to test the timeout path.
+extern "C" GPTQ_API int gptq_internal_dequant_stalled(const int32_t* qweight, const int32_t* qzeros,
+                                                      const float* scales, const int32_t* g_idx,
+                                                      int64_t d_row, int64_t d_col, int32_t bits,
+                                                      int32_t group_size, void* W_out,
+                                                      unsigned long long wait_ns,
+                                                      gptq_stream_t stream) {
+  if (!qweight || !qzeros || !scales || !g_idx || !W_out || d_row < 32 || d_row % 32 || d_col < 32 ||
+      d_col % 32 || (bits != 2 && bits != 3 && bits != 4 && bits != 8) || wait_ns == 0)
+    return GPTQ_ERR_INVALID_ARG;
+  const int n_groups = group_size == -1 ? 1 : static_cast<int>(d_col / group_size);
+  return gptq::launch_dequant_impl(qweight, qzeros, scales, g_idx, d_row, d_col, bits, n_groups,
+                                   GPTQ_W_FP16, W_out, reinterpret_cast<cudaStream_t>(stream), 1,
+                                   wait_ns);
+}

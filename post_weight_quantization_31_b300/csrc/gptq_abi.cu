@@ -2,6 +2,7 @@
 // read-back, and the sticky device fault word.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -11,17 +12,22 @@ uint64_t g_launches = 0;
 
 __device__ int g_fault_word = 0;
 
+namespace {
+std::mutex g_fault_mu;
+int* g_fault_addr[64] = {nullptr};
+}  // namespace
+
 int* fault_word_ptr() {
-  // One address per device; the symbol lives in this library's module.
-  static int* cache[64] = {nullptr};
+  // One address per device (the symbol lives in this library's module),
+  // looked up on first use with that device current.
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_fault_mu);
+  if (!g_fault_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fault_word) == cudaSuccess) cache[dev] = static_cast<int*>(p);
+    if (cudaGetSymbolAddress(&p, g_fault_word) == cudaSuccess) g_fault_addr[dev] = static_cast<int*>(p);
   }
-  return cache[dev];
+  return g_fault_addr[dev];
 }
 
 gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, float* S,
@@ -30,13 +36,12 @@ gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t
                                 cudaStream_t st);
 size_t prep_workspace_bytes(int64_t d);
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d, int64_t n_seen, float damp,
-                             bool desc_act, float* U, int32_t* perm, void* ws, cudaStream_t st,
-                             int* status_host);
+                             bool desc_act, float* U, int32_t* perm, void* ws, cudaStream_t st);
 size_t quant_workspace_bytes(int64_t d_row, int64_t d_col);
 gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row, int64_t d_col, const float* U,
                               const int32_t* perm, const gptq_config_t& cfg, uint8_t* codes,
                               float* scales, uint8_t* zeros, int32_t* g_idx, void* ws,
-                              cudaStream_t st, int* status_host);
+                              cudaStream_t st);
 gptq_status_t launch_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,
                           int bits, int n_groups, int32_t* qweight, int32_t* qzeros, cudaStream_t st);
 gptq_status_t launch_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row, int64_t d_col,
@@ -58,14 +63,16 @@ bool bits_ok(int bits) { return bits == 2 || bits == 3 || bits == 4 || bits == 8
 bool config_ok(const gptq_config_t* c, int64_t d_col) {
   if (!c) return false;
   if (!bits_ok(c->bits)) return false;
-  if (c->blocksize != 128) return false;
+  // The lazy-batch width only orders the same sums differently; the kernels
+  // run their own 128 / 512-column blocking, whatever this value is.
+  if (c->blocksize < 32 || c->blocksize % 32 != 0) return false;
   if (!(c->damp_percent >= 0.f) || !std::isfinite(c->damp_percent)) return false;
   if (c->desc_act != 0 && c->desc_act != 1) return false;
   if (c->sym != 0 && c->sym != 1) return false;
   const int gs = c->group_size;
   if (gs == -1) return true;
   if (gs <= 0 || gs % 32 != 0) return false;
-  if (c->blocksize % gs != 0) return false;
+  if (128 % gs != 0) return false;   // a group lies inside one 128-column block of the kernels
   if (d_col % gs != 0) return false;
   return true;
 }
@@ -82,28 +89,42 @@ int n_groups_of(int group_size, int64_t d_col) {
   return group_size == -1 ? 1 : static_cast<int>(d_col / group_size);
 }
 
-// Reads (and clears) the sticky fault word; synchronizes the stream.
-gptq_status_t finish(cudaStream_t st, int status_word) {
-  int fault = 0;
-  int* fw = fault_word_ptr();
-  if (fw) {
-    if (cudaMemcpyAsync(&fault, fw, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return GPTQ_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return GPTQ_ERR_CUDA;
-    if (fault) {
-      const int zero = 0;
-      cudaMemcpyAsync(fw, &zero, sizeof(int), cudaMemcpyHostToDevice, st);
-      cudaStreamSynchronize(st);
-      return GPTQ_ERR_TIMEOUT;
-    }
-  } else if (cudaStreamSynchronize(st) != cudaSuccess) {
-    return GPTQ_ERR_CUDA;
-  }
-  if (status_word & kStatTimeout) return GPTQ_ERR_TIMEOUT;
-  if (status_word & kStatNonFinite) return GPTQ_ERR_NONFINITE;
-  if (status_word & kStatNotPD) return GPTQ_ERR_NOT_PD;
+gptq_status_t status_of_bits(int bits) {
+  if (bits & kStatTimeout) return GPTQ_ERR_TIMEOUT;
+  if (bits & kStatNonFinite) return GPTQ_ERR_NONFINITE;
+  if (bits & kStatNotPD) return GPTQ_ERR_NOT_PD;
   return GPTQ_OK;
 }
+
+// Reads (and clears) the library's sticky fault word; synchronizes the stream.
+gptq_status_t read_fault_word(cudaStream_t st) {
+  int fault = 0;
+  int* fw = fault_word_ptr();
+  if (!fw) return GPTQ_ERR_CUDA;
+  if (cudaMemcpyAsync(&fault, fw, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GPTQ_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GPTQ_ERR_CUDA;
+  if (fault) {
+    if (cudaMemsetAsync(fw, 0, sizeof(int), st) != cudaSuccess) return GPTQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GPTQ_ERR_CUDA;
+    return GPTQ_ERR_TIMEOUT;
+  }
+  return GPTQ_OK;
+}
+
+}  // namespace
+
+// The status word a prepare or quantize call leaves at the start of its
+// workspace (offset 0 in both workspace layouts); synchronizes the stream.
+gptq_status_t read_workspace_status(const void* ws, cudaStream_t st) {
+  int bits = 0;
+  if (cudaMemcpyAsync(&bits, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return GPTQ_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return GPTQ_ERR_CUDA;
+  return status_of_bits(bits);
+}
+
+namespace {
 
 }  // namespace
 }  // namespace gptq
@@ -147,11 +168,8 @@ gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int64_t d_co
   if (!ws || !aligned(ws, 256) || ws_bytes < prep_workspace_bytes(d_col)) return GPTQ_ERR_WORKSPACE;
   if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int status = 0;
-  gptq_status_t s = launch_prepare(S, diag, d_col, n_seen, cfg->damp_percent, cfg->desc_act != 0, U,
-                                   perm, ws, st, &status);
-  if (s != GPTQ_OK) return s;
-  return finish(st, status);
+  return launch_prepare(S, diag, d_col, n_seen, cfg->damp_percent, cfg->desc_act != 0, U, perm, ws,
+                        st);
 }
 
 size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const gptq_config_t* cfg) {
@@ -175,11 +193,8 @@ gptq_status_t gptq_quantize_layer(const void* W, int32_t w_dtype, int64_t d_row,
     return GPTQ_ERR_WORKSPACE;
   if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  int status = 0;
-  gptq_status_t s = launch_quantize(W, w_dtype, d_row, d_col, U, perm, *cfg, codes, scales, zeros,
-                                    g_idx, ws, st, &status);
-  if (s != GPTQ_OK) return s;
-  return finish(st, status);
+  return launch_quantize(W, w_dtype, d_row, d_col, U, perm, *cfg, codes, scales, zeros, g_idx, ws,
+                         st);
 }
 
 gptq_status_t gptq_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,
@@ -264,7 +279,12 @@ const char* gptq_status_string(gptq_status_t s) {
 }
 
 gptq_status_t gptq_device_fault(gptq_stream_t stream) {
-  return finish(reinterpret_cast<cudaStream_t>(stream), 0);
+  return read_fault_word(reinterpret_cast<cudaStream_t>(stream));
+}
+
+gptq_status_t gptq_workspace_status(const void* ws, gptq_stream_t stream) {
+  if (!ws || !aligned(ws, 256)) return GPTQ_ERR_INVALID_ARG;
+  return read_workspace_status(ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 uint64_t gptq_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }

@@ -634,7 +634,7 @@ size_t prep_workspace_bytes(int64_t d) { return prep_layout(d).total; }
 
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, int64_t n_seen,
                              float damp, bool desc_act, float* U, int32_t* perm, void* ws,
-                             cudaStream_t st, int* status_host) {
+                             cudaStream_t st) {
   const int d = static_cast<int>(d64);
   const PrepLayout L = prep_layout(d64);
   char* base = static_cast<char*>(ws);
@@ -702,11 +702,10 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
       g.diag_lo = zlo;
       const gptq_status_t s = launch_tgemm_3xtf32(Bhi + static_cast<int64_t>(k + b) * NB,
                                                   Blo + static_cast<int64_t>(k + b) * NB, NB, Bhi, Blo,
-                                                  NB, g, st);
+                                                  NB, g, status, st);
       if (s != GPTQ_OK) return s;
     }
   }
-  GPTQ_CUDA_TRY(cudaMemcpyAsync(status_host, status, sizeof(int), cudaMemcpyDeviceToHost, st));
   return GPTQ_OK;
 }
 

@@ -14,6 +14,7 @@
 namespace gptq {
 
 size_t prep_workspace_bytes(int64_t d);
+gptq_status_t read_workspace_status(const void* ws, cudaStream_t st);
 
 namespace {
 
@@ -56,5 +57,10 @@ extern "C" GPTQ_API gptq_status_t gptq_prepare_hinv_noalloc(const float* S, cons
   if (d_col > 0 && gptq::prep_workspace_bytes(d_col) > gptq::kScratchBytes) return GPTQ_ERR_WORKSPACE;
   void* ws = gptq::scratch_address();
   if (!ws) return GPTQ_ERR_CUDA;
-  return gptq_prepare_hinv(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream);
+  const gptq_status_t s =
+      gptq_prepare_hinv(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream);
+  if (s != GPTQ_OK) return s;
+  // The status word of the call sits in the library's array, where the
+  // caller cannot read it: wait for the call and report it here.
+  return gptq::read_workspace_status(ws, reinterpret_cast<cudaStream_t>(stream));
 }

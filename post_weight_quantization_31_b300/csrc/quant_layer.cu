@@ -376,7 +376,7 @@ size_t quant_workspace_bytes(int64_t d_row, int64_t d_col) { return quant_layout
 gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64_t d_col64,
                               const float* U, const int32_t* perm, const gptq_config_t& cfg,
                               uint8_t* codes, float* scales, uint8_t* zeros, int32_t* g_idx,
-                              void* ws, cudaStream_t st, int* status_host) {
+                              void* ws, cudaStream_t st) {
   const int d_row = static_cast<int>(d_row64), d_col = static_cast<int>(d_col64);
   const QuantLayout L = quant_layout(d_row64, d_col64);
   char* base = static_cast<char*>(ws);
@@ -436,7 +436,7 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
     g.col_off = 0;
     return launch_tgemm_3xtf32(Err_hi + e0, Err_lo + e0, SB,
                                Ut_hi + static_cast<int64_t>(n0) * d_col + k0,
-                               Ut_lo + static_cast<int64_t>(n0) * d_col + k0, d_col, g, st);
+                               Ut_lo + static_cast<int64_t>(n0) * d_col + k0, d_col, g, status, st);
   };
   for (int sb0 = 0; sb0 < d_col; sb0 += SB) {
     const int sb1 = std::min(sb0 + SB, d_col);
@@ -474,7 +474,6 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
       if (s != GPTQ_OK) return s;
     }
   }
-  GPTQ_CUDA_TRY(cudaMemcpyAsync(status_host, status, sizeof(int), cudaMemcpyDeviceToHost, st));
   return GPTQ_OK;
 }
 

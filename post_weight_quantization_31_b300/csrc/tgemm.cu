@@ -310,8 +310,9 @@ TGemmSched make_sched(const TGemmArgs& a) {
 int tgemm_tile_count(const TGemmArgs& args) { return make_sched(args).tiles; }
 
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
-                                  const float* B_lo, int64_t ldb, const TGemmArgs& args,
+                                  const float* B_lo, int64_t ldb, const TGemmArgs& args, int* fault,
                                   cudaStream_t st) {
+  if (!fault) return GPTQ_ERR_CUDA;
   if (args.M <= 0 || args.N <= 0 || args.K <= 0) return GPTQ_OK;
   const TGemmSched s = make_sched(args);
   if (s.tiles == 0) return GPTQ_OK;
@@ -329,7 +330,7 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
   }
   const int grid = std::min(sm_count(), s.tiles);
   GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, m_ahi, m_alo,
-                           m_bhi, m_blo, args, s, fault_word_ptr()));
+                           m_bhi, m_blo, args, s, fault));
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
@@ -354,6 +355,6 @@ extern "C" GPTQ_API int gptq_internal_tgemm(const float* A_hi, const float* A_lo
   g.lower = lower;
   g.row_off = row_off;
   g.col_off = col_off;
-  return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g,
+  return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g, gptq::fault_word_ptr(),
                                    reinterpret_cast<cudaStream_t>(stream));
 }

@@ -47,9 +47,11 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   lo = round_tf32(__fsub_rn(x, hi));
 }
 
+// `fault`: the status word the kernel's bounded waits report a timeout in
+// (and read to stop early once one has run out).
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda,
                                   const float* B_hi, const float* B_lo, int64_t ldb,
-                                  const TGemmArgs& args, cudaStream_t st);
+                                  const TGemmArgs& args, int* fault, cudaStream_t st);
 
 // Number of 128 x 128 output tiles the launch above would process.
 int tgemm_tile_count(const TGemmArgs& args);

@@ -56,6 +56,7 @@ def gpu_solve(W: np.ndarray, w_dtype: str, X: np.ndarray, cfg, chunks: int = 1,
     solver.prepare()
     solver.quantize(torch_w(W, w_dtype))
     solver.pack()
+    solver.check()
     torch.cuda.synchronize()
     o = solver.out
     return GpuOut(codes=o["codes"].cpu().numpy().astype(np.int64),
@@ -149,6 +150,7 @@ def assert_parity(m: dict, scale_rtol: float = SCALE_RTOL) -> None:
     assert m["code_maxdiff"] <= 1, m
     assert m["zero_match"] >= CODE_MATCH, m
     assert m["zero_maxdiff"] <= 1, m
+    assert m["upstream_frac"] >= CODE_MATCH, m
     assert m["scale_rel"] <= scale_rtol, m
     assert m["recon_rel"] <= RECON_RTOL, m
 

@@ -81,7 +81,8 @@ def test_accumulate_rejects_null_and_misaligned(lib):
 
 
 @pytest.mark.parametrize("kw", [dict(bits=5), dict(bits=1), dict(group_size=48),
-                                dict(group_size=256), dict(group_size=0), dict(blocksize=64),
+                                dict(group_size=256), dict(group_size=0), dict(blocksize=48),
+                                dict(blocksize=0), dict(blocksize=-32),
                                 dict(damp_percent=-0.1), dict(desc_act=2), dict(sym=3),
                                 dict(damp_percent=float("nan"))])
 def test_prepare_rejects_bad_config(lib, kw):

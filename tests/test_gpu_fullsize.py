@@ -2,15 +2,13 @@
 in the configuration the benchmark times (one accumulate over all tokens,
 then prepare, quantize and pack through the C ABI).
 
-The oracle cannot redo a whole 4096 x 11008 layer in seconds, so:
-  * where its fp64 Hessian fits in time (d_col 4096), it solves a seeded
-    sample of rows exactly (rows are independent) with its own S and U;
-  * at d_col 11008 and 13824 with all tokens, it checks what it can compute
-    one by one: sampled entries of S, the act-order permutation from its
-    exact diagonal, and U^T U h_j = e_j for exact columns h_j of the damped
-    Hessian; then it solves sampled rows exactly at the same d_col with a
-    shorter calibration set (same distribution).
-Tolerances are those of the other parity tests (tests/parity.py).
+Every layer shape of the five calibration workloads is covered.  The oracle
+cannot redo a whole layer's column loop in seconds, so for each shape it
+builds its own fp64 S from all tokens and its own U, compares them with the
+GPU's S (whole matrix), order and U, and then solves a seeded sample of rows
+exactly (rows are independent): codes, scales, zeros, reconstruction error
+and packing of those rows against the GPU's.  Tolerances are those of the
+other parity tests (tests/parity.py), with no case held to a lower bar.
 """
 import numpy as np
 import pytest
@@ -44,6 +42,7 @@ def gpu_layer(inp, exact_diag=None, want_S=False, want_U=False):
     solver.prepare()
     solver.quantize(P.torch_w(inp.W, inp.w_dtype))
     solver.pack()
+    solver.check()
     torch.cuda.synchronize()
     o = solver.out
     res = dict(codes=o["codes"].cpu().numpy(), scales=o["scales"].cpu().numpy(),
@@ -65,7 +64,7 @@ def sample_rows(d_row, k, seed):
     return np.sort(rng.choice(d_row, size=k, replace=False))
 
 
-def check_rows_exact(inp, g, S64, perm, U, rows, code_match=P.CODE_MATCH):
+def check_rows_exact(inp, g, S64, perm, U, rows):
     """Oracle column loop on the sampled rows with the oracle's own U; the
     GPU's codes, scales, zeros and reconstruction error must agree."""
     cfg = inp.cfg
@@ -77,13 +76,17 @@ def check_rows_exact(inp, g, S64, perm, U, rows, code_match=P.CODE_MATCH):
     Q[:, perm] = Q_p
     gc = g["codes"][rows].astype(np.int64)
     same = gc == codes
-    assert same.mean() >= code_match, same.mean()
+    assert same.mean() >= P.CODE_MATCH, same.mean()
     assert np.abs(gc - codes).max() <= 1
     gs, gz = g["scales"][:, rows], g["zeros"][:, rows]
     up = P.upstream_groups(gc, codes, perm, cfg.group_size, scales.shape[0])
+    # the scale check covers the groups upstream of any code difference, and
+    # those must be nearly all of them
+    assert up.mean() >= P.CODE_MATCH, up.mean()
     srel = np.abs(gs.astype(np.float64) - scales) / np.abs(scales.astype(np.float64))
     assert srel[up].max() <= P.SCALE_RTOL, srel[up].max()
-    assert (gz == zeros).mean() >= code_match
+    assert (gz == zeros).mean() >= P.CODE_MATCH
+    assert np.abs(gz - zeros).max() <= 1
     eg = P.output_error(inp.W[rows], P.dequantized(gc, gs, gz, g["g_idx"]), S64)
     er = O.recon_error(inp.W[rows], Q, S64)
     assert abs(eg - er) / er <= P.RECON_RTOL, (eg, er)
@@ -91,103 +94,52 @@ def check_rows_exact(inp, g, S64, perm, U, rows, code_match=P.CODE_MATCH):
     assert np.array_equal(P.unpack_columns(g["qweight"][:, rows], cfg.bits, W.shape[1]), gc)
 
 
-def check_hessian_samples(X, S_gpu, n, seed):
-    rng = np.random.Generator(np.random.PCG64(seed))
-    d = X.shape[0]
-    dg = np.diag(S_gpu).astype(np.float64)
-    for _ in range(48):
-        i, j = (int(v) for v in rng.integers(0, d, size=2))
-        want = O.hessian_entry(X, i, j)
-        scale = np.sqrt(O.hessian_entry(X, i, i) * O.hessian_entry(X, j, j))
-        assert abs(float(S_gpu[i, j]) - want) / scale < P.s_tol(n), (i, j)
-    assert np.all(dg > 0)
+# ------------------------------------------------------------------ all shapes
+# (id, inputs, exact fp64 diagonal as the benchmark or API default runs it,
+#  sampled rows, key of the calibration set: cases with the same X share the
+#  oracle's S and U, which do not depend on bits)
+CASES = [
+    ("attn_proj_7b", lambda: wl.attn_proj_7b(), False, 48, "attn7b"),
+    ("mlp_gate_up_7b", lambda: wl.mlp_7b("gate_up"), None, 32, "mlp_gu"),
+    ("mlp_down_7b", lambda: wl.mlp_7b("down"), None, 32, "mlp_down"),
+    ("decoder_qkv_7b", lambda: wl.decoder_site_7b("qkv", layer=0), None, 48, "dec_qkv"),
+    ("decoder_o_7b", lambda: wl.decoder_site_7b("o", layer=0), None, 48, "dec_o"),
+    ("decoder_gate_up_7b", lambda: wl.decoder_site_7b("gate_up", layer=0), None, 32, "dec_gu"),
+    ("decoder_down_7b", lambda: wl.decoder_site_7b("down", layer=0), None, 32, "dec_down"),
+    ("lowbit_attn_13b_3bit", lambda: wl.lowbit_13b("attn", 3), None, 32, "l13_attn"),
+    ("lowbit_attn_13b_2bit", lambda: wl.lowbit_13b("attn", 2), None, 32, "l13_attn"),
+    ("lowbit_gate_up_13b_3bit", lambda: wl.lowbit_13b("gate_up", 3), None, 32, "l13_gu"),
+    ("lowbit_gate_up_13b_2bit", lambda: wl.lowbit_13b("gate_up", 2), None, 32, "l13_gu"),
+    ("lowbit_down_13b_3bit", lambda: wl.lowbit_13b("down", 3), None, 32, "l13_down"),
+    ("lowbit_down_13b_2bit", lambda: wl.lowbit_13b("down", 2), None, 32, "l13_down"),
+]
+
+_CACHE = {}
 
 
-# ------------------------------------------------------------------ d_col 4096
-@pytest.mark.parametrize("case", ["attn_proj_7b", "decoder_qkv_7b"])
-def test_full_size_exact_on_sampled_rows(case):
-    if case == "attn_proj_7b":
-        inp = wl.attn_proj_7b()              # the benchmark workload
-        exact_diag = False                   # as bench.py runs it
-    else:
-        inp = wl.decoder_site_7b("qkv", layer=0)
-        exact_diag = None
-    g = gpu_layer(inp, exact_diag=exact_diag, want_S=True, want_U=True)
+def _oracle_factor(key, inp):
+    """The oracle's fp64 S from all tokens, its order and its U, shared by
+    the cases with the same calibration set."""
+    if key not in _CACHE:
+        _CACHE.clear()
+        S64 = O.hessian_sum_chunked(inp.X)
+        perm, _Hp, U = O.prepare(S64, inp.X.shape[1], inp.cfg)
+        _CACHE[key] = (S64, perm, U)
+    return _CACHE[key]
+
+
+@pytest.mark.parametrize("name,make,exact_diag,nrows,key", CASES, ids=[c[0] for c in CASES])
+def test_full_size_layer_against_oracle(name, make, exact_diag, nrows, key):
+    inp = make()
     n = inp.X.shape[1]
-    S64 = O.hessian_sum_chunked(inp.X)
+    g = gpu_layer(inp, exact_diag=exact_diag, want_S=True, want_U=True)
+    S64, perm, U = _oracle_factor(key, inp)
     assert P.s_error(g["S"], S64) < P.s_tol(n)
-    perm, _Hp, U = O.prepare(S64, n, inp.cfg)
     assert np.array_equal(g["perm"], perm)
     assert np.array_equal(g["g_idx"], O.group_index(perm, inp.cfg.group_size))
     Ug = g["U"].astype(np.float64)
     assert np.all(np.tril(Ug, -1) == 0) and np.all(np.diag(Ug) > 0)
     assert np.max(np.abs(Ug - U)) / np.max(np.abs(U)) < 2e-4
-    rows = sample_rows(inp.W.shape[0], 48, seed=7)
+    assert g["codes"].max() <= (1 << inp.cfg.bits) - 1
+    rows = sample_rows(inp.W.shape[0], nrows, seed=17)
     check_rows_exact(inp, g, S64, perm, U, rows)
-
-
-# ------------------------------------------------------------------ d_col 11008 / 13824
-WIDE = [
-    ("mlp_down_7b", lambda n: wl.mlp_7b("down", n_tok=n), 262144),
-    ("lowbit_down_13b_3bit", lambda n: wl.lowbit_13b("down", 3, n_tok=n), 131072),
-]
-
-
-@pytest.mark.parametrize("name,make,n_full", WIDE, ids=[w[0] for w in WIDE])
-def test_wide_layer_properties_at_full_tokens(name, make, n_full):
-    inp = make(n_full)
-    g = gpu_layer(inp, want_S=True, want_U=True)
-    X, n, cfg = inp.X, inp.X.shape[1], inp.cfg
-    check_hessian_samples(X, g["S"], n, seed=11)
-    hdiag = (2.0 / n) * O.hessian_diag(X)
-    perm = O.act_order_diag(hdiag, cfg.desc_act)
-    assert np.array_equal(g["perm"], perm)
-    lam = cfg.damp_percent * float(np.mean(hdiag))
-    U = g["U"].astype(np.float64)
-    assert np.all(np.tril(U, -1) == 0) and np.all(np.diag(U) > 0)
-    rng = np.random.Generator(np.random.PCG64(12))
-    js = np.sort(rng.choice(X.shape[0], size=3, replace=False))   # processing positions
-    cols = (2.0 / n) * O.hessian_columns(X, perm[js])               # H[:, perm[j]]
-    for c, j in enumerate(js):
-        h = cols[perm, c].copy()                                    # column j of Hp
-        h[j] += lam
-        r = U.T @ (U @ h)
-        e = np.zeros_like(r)
-        e[j] = 1.0
-        assert np.max(np.abs(r - e)) < 5e-3, (name, j, np.max(np.abs(r - e)))
-    # codes are valid levels and pack exactly
-    assert g["codes"].max() <= (1 << cfg.bits) - 1
-    rows = sample_rows(inp.W.shape[0], 8, seed=13)
-    assert np.array_equal(P.unpack_columns(g["qweight"][:, rows], cfg.bits, X.shape[0]),
-                          g["codes"][rows].astype(np.int64))
-
-
-_WIDE_CACHE = {}
-
-
-def _wide_oracle(key, inp):
-    """The oracle's fp64 Hessian and factor, shared by the cases with the same X."""
-    if key not in _WIDE_CACHE:
-        _WIDE_CACHE.clear()
-        S64 = O.hessian_sum_chunked(inp.X)
-        perm, _Hp, U = O.prepare(S64, inp.X.shape[1], inp.cfg)
-        _WIDE_CACHE[key] = (S64, perm, U)
-    return _WIDE_CACHE[key]
-
-
-EXACT_WIDE = [
-    # (id, inputs, oracle cache key, code-match floor)
-    ("mlp_down_7b", lambda: wl.mlp_7b("down"), "mlp_down", P.CODE_MATCH),
-    ("lowbit_down_13b_2bit", lambda: wl.lowbit_13b("down", 2), "down13b", P.CODE_MATCH),
-    ("lowbit_down_13b_3bit", lambda: wl.lowbit_13b("down", 3), "down13b", 0.998),
-]
-
-
-@pytest.mark.parametrize("name,make,key,floor", EXACT_WIDE, ids=[w[0] for w in EXACT_WIDE])
-def test_wide_layer_exact_on_sampled_rows(name, make, key, floor):
-    inp = make()
-    g = gpu_layer(inp)
-    S64, perm, U = _wide_oracle(key, inp)   # damping and order do not depend on bits
-    assert np.array_equal(g["perm"], perm)
-    rows = sample_rows(inp.W.shape[0], 32, seed=17)
-    check_rows_exact(inp, g, S64, perm, U, rows, code_match=floor)

@@ -112,6 +112,9 @@ CASES = [
     (64, 1024, 4096, "bf16", dict(group_size=-1, desc_act=True)),
     (96, 544, 2088, "bf16", dict(group_size=32)),          # ragged last block and tokens
     (64, 640, 1500, "fp32", dict(bits=3, group_size=-1, sym=True)),
+    # other lazy-batch widths: the oracle batches by them, the GPU by its own blocks
+    (64, 1024, 4096, "bf16", dict(blocksize=32)),
+    (64, 1024, 4096, "bf16", dict(blocksize=256, group_size=64, desc_act=True)),
 ]
 
 
@@ -127,22 +130,24 @@ def test_layer_parity(d_row, d_col, n_tok, w_dtype, kw):
     assert np.array_equal(P.unpack_columns(g.qweight, cfg.bits, W.shape[1]), g.codes)
 
 
-def test_correlated_inputs_quality():
-    """Strongly correlated X: free-running codes may cascade apart from the
-    oracle's, so the check is on what is unique (the order) and on the
-    quality of the result: the GPU's reconstruction error within 2% of the
-    oracle's and below round-to-nearest."""
-    cfg = qc(group_size=64, desc_act=True)
-    X = wl.make_correlated_activations(512, 2048, seed=77)
+@pytest.mark.parametrize("kind,bits,gs,sym", [("correlated", 4, 64, False),
+                                              ("correlated", 3, 64, True),
+                                              ("lowrank", 4, 128, False)])
+def test_strongly_correlated_inputs(kind, bits, gs, sym):
+    """X far from i.i.d.: a dense mixing matrix (X = A Z) or low rank plus
+    noise, so that H is far from diagonal and the error feedback, not the
+    rounding alone, decides the result.  Held to the same bar as every
+    other case: codes, zeros, scales and reconstruction error."""
+    cfg = qc(bits=bits, group_size=gs, sym=sym, desc_act=True)
+    if kind == "correlated":
+        X = wl.make_correlated_activations(512, 2048, seed=77)
+    else:
+        X = wl.make_lowrank_activations(512, 2048, seed=79)
     W = wl.make_weight(64, 512, seed=78, dtype="bf16")
-    g = P.gpu_solve(W, "bf16", X, cfg)
-    S64 = O.hessian_sum(X)
-    free = O.quantize_layer(W, S64, X.shape[1], cfg)
-    assert np.array_equal(g.perm, free.perm)
-    eg = P.output_error(W, P.dequantized(g.codes, g.scales, g.zeros, g.g_idx), S64)
-    ef = O.recon_error(W, free.Q, S64)
-    assert abs(eg - ef) / ef <= 0.02
-    assert eg < O.recon_error(W, O.rtn(W, cfg).Q, S64)
+    g, ref, S64, m = run_case(W, "bf16", X, cfg)
+    P.assert_parity(m)
+    assert m["upstream_frac"] >= P.CODE_MATCH, m
+    assert m["recon_gpu"] < O.recon_error(W, O.rtn(W, cfg).Q, S64)
 
 
 def test_identity_hessian_gives_rtn():
