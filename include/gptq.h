@@ -127,9 +127,15 @@ enum { GPTQ_W_FP32 = 0, GPTQ_W_BF16 = 1, GPTQ_W_FP16 = 2 };
 /*
  * a1  S += X X^T   ([G] §2.1: the Hessian is computed from the layer's
  *                   calibration activations; H = 2/n S is formed in a2.)
- *   X       fp16 [d_col, n_tok] with row stride ldx elements (tokens
- *           contiguous).  16-byte aligned, ldx >= n_tok, ldx % 8 == 0.
- *           Read only.
+ *   X       fp16, read only, 16-byte aligned, ldx % 8 == 0:
+ *           x_token_major = 0: [d_col, n_tok] with row stride ldx elements
+ *             (tokens contiguous), ldx >= n_tok;
+ *           x_token_major = 1: [n_tok, d_col] with row stride ldx elements
+ *             (channels contiguous, the layout of a [tokens, features]
+ *             activation tensor), ldx >= d_col.
+ *           Both layouts feed the tensor cores directly (K-major or
+ *           MN-major operand tiles); the result is the same up to the order
+ *           of fp32 additions.
  *   S       fp32 [d_col, d_col], row-major, 16-byte aligned, updated in place
  *           with the full symmetric product (both triangles).  Zero it
  *           before the first call; call once per chunk of tokens.
@@ -146,8 +152,8 @@ enum { GPTQ_W_FP32 = 0, GPTQ_W_BF16 = 1, GPTQ_W_FP16 = 2 };
  *   the last bits of S, can differ from run to run.  Asynchronous.
  */
 GPTQ_API gptq_status_t gptq_hessian_accumulate(const void* X, int64_t d_col, int64_t n_tok,
-                                      int64_t ldx, float* S, double* diag, int64_t* n_seen,
-                                      gptq_stream_t stream);
+                                               int64_t ldx, int32_t x_token_major, float* S,
+                                               double* diag, int64_t* n_seen, gptq_stream_t stream);
 
 /* Bytes of workspace gptq_prepare_hinv needs for d_col. */
 GPTQ_API size_t gptq_prepare_workspace_size(int64_t d_col);

@@ -38,7 +38,7 @@ class GptqConfigC(ctypes.Structure):
 _CFGP = ctypes.POINTER(GptqConfigC)
 
 SIGNATURES = {
-    "gptq_hessian_accumulate": (_i32, [_vp, _i64, _i64, _i64, _vp, _vp,
+    "gptq_hessian_accumulate": (_i32, [_vp, _i64, _i64, _i64, _i32, _vp, _vp,
                                        ctypes.POINTER(ctypes.c_int64), _vp]),
     "gptq_prepare_workspace_size": (_sz, [_i64]),
     "gptq_prepare_hinv": (_i32, [_vp, _vp, _i64, _i64, _CFGP, _vp, _vp, _vp, _sz, _vp]),

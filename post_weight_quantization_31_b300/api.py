@@ -59,28 +59,32 @@ def launch_count() -> int:
 
 
 # ----------------------------------------------------------------------- a1
-def hessian_accumulate(X: torch.Tensor, S: torch.Tensor, diag: torch.Tensor | None = None) -> int:
+def hessian_accumulate(X: torch.Tensor, S: torch.Tensor, diag: torch.Tensor | None = None,
+                       token_major: bool = False) -> int:
     """S += X X^T (and diag += sum_t X^2 in fp64 if given).  X: fp16
-    [d_col, n_tok] with unit stride along tokens.  Returns n_tok."""
+    [d_col, n_tok] with unit stride along tokens, or with token_major=True
+    [n_tok, d_col] with unit stride along channels (a [tokens, features]
+    activation tensor).  Returns n_tok."""
     lib = _lib.load()
     _need(X, torch.float16, "X")
     if X.dim() != 2 or X.stride(1) != 1:
-        raise ValueError("X must be 2-D with tokens contiguous")
-    d_col, n_tok = X.shape
+        raise ValueError("X must be 2-D with a unit inner stride")
+    n_tok, d_col = X.shape if token_major else X.shape[::-1]
     if X.stride(0) % 8 != 0 or X.data_ptr() % 16 != 0:
         # The library reads X with TMA, which needs 16-byte aligned rows:
         # copy into storage whose row stride is a multiple of 8 halves.
-        ld = (n_tok + 7) // 8 * 8
-        Xp = torch.empty((d_col, ld), dtype=X.dtype, device=X.device)
-        Xp[:, :n_tok].copy_(X)
-        X = Xp[:, :n_tok]
+        rows, cols = X.shape
+        ld = (cols + 7) // 8 * 8
+        Xp = torch.empty((rows, ld), dtype=X.dtype, device=X.device)
+        Xp[:, :cols].copy_(X)
+        X = Xp[:, :cols]
     _need(S, torch.float32, "S", (d_col, d_col))
     _contig(S, "S")
     if diag is not None:
         _need(diag, torch.float64, "diag", (d_col,))
     n = ctypes.c_int64(0)
-    _check(lib.gptq_hessian_accumulate(X.data_ptr(), d_col, n_tok, X.stride(0), S.data_ptr(),
-                                       _ptr(diag), ctypes.byref(n), _stream()),
+    _check(lib.gptq_hessian_accumulate(X.data_ptr(), d_col, n_tok, X.stride(0), int(token_major),
+                                       S.data_ptr(), _ptr(diag), ctypes.byref(n), _stream()),
            "gptq_hessian_accumulate")
     return int(n.value)
 

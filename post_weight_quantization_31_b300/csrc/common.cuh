@@ -228,6 +228,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand tile in the 128-byte-swizzle canonical
+// layout: 128-byte rows hold 64 consecutive M (or N) elements of one k, 8
+// rows (8 k) form a 1024-byte atom; lbo = byte stride between the 64-element
+// chunks along M/N, sbo = byte stride between the 8-k groups (bits 16-29
+// and 32-45, both >> 4).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mnmajor(uint32_t saddr, uint32_t lbo,
+                                                            uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32: D fp32, both operands
 // K-major, shape M x N.  a_fmt/b_fmt: 0 = f16, 1 = bf16, 2 = tf32.
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_fmt, int b_fmt,

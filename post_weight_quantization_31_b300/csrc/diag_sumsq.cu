@@ -73,12 +73,61 @@ __global__ void __launch_bounds__(DS_THREADS)
   }
 }
 
+// Token-major X [n_tok][ldx] (channels contiguous): each thread owns 8
+// consecutive channels (one 16-byte load per token, a warp covers 256
+// channels of a token row), the 8 warps of a block take interleaved tokens
+// of the block's chunk, and the warps' partials are combined in fp64.
+constexpr int DT_WARPS = 8;
+constexpr int DT_TOK = 2048;   // tokens per block
+
+__global__ void __launch_bounds__(DT_WARPS * 32)
+    diag_sumsq_tokmajor_kernel(const __half* __restrict__ X, int64_t d, int64_t n_tok, int64_t ldx,
+                               double* __restrict__ diag) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 256 + lane * 8;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * DT_TOK;
+  const int64_t t1 = t0 + DT_TOK < n_tok ? t0 + DT_TOK : n_tok;
+  DF acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = DF{0.f, 0.f};
+  if (c0 < d) {  // d is a multiple of 8: a thread's 8 channels are all in range or all out
+    for (int64_t t = t0 + warp; t < t1; t += DT_WARPS) {
+      const uint4 u = *reinterpret_cast<const uint4*>(X + t * ldx + c0);
+      const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(h[k]);
+        df_add(acc[2 * k], __fmul_rn(f.x, f.x));
+        df_add(acc[2 * k + 1], __fmul_rn(f.y, f.y));
+      }
+    }
+  }
+  __shared__ double red[DT_WARPS][256];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    red[warp][lane * 8 + k] = static_cast<double>(acc[k].hi) + static_cast<double>(acc[k].lo);
+  __syncthreads();
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (c < d) {
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < DT_WARPS; ++w) tot += red[w][threadIdx.x];
+    atomicAdd(diag + c, tot);
+  }
+}
+
 }  // namespace
 
-gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t ldx, double* diag,
-                                cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(d), static_cast<unsigned>((n_tok + DS_CHUNK - 1) / DS_CHUNK));
-  diag_sumsq_kernel<<<grid, DS_THREADS, 0, st>>>(static_cast<const __half*>(X), n_tok, ldx, diag);
+gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t ldx, bool tok_major,
+                                double* diag, cudaStream_t st) {
+  if (tok_major) {
+    dim3 grid(static_cast<unsigned>((d + 255) / 256), static_cast<unsigned>((n_tok + DT_TOK - 1) / DT_TOK));
+    diag_sumsq_tokmajor_kernel<<<grid, DT_WARPS * 32, 0, st>>>(static_cast<const __half*>(X), d, n_tok,
+                                                                ldx, diag);
+  } else {
+    dim3 grid(static_cast<unsigned>(d), static_cast<unsigned>((n_tok + DS_CHUNK - 1) / DS_CHUNK));
+    diag_sumsq_kernel<<<grid, DS_THREADS, 0, st>>>(static_cast<const __half*>(X), n_tok, ldx, diag);
+  }
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }

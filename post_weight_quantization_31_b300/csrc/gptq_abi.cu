@@ -30,10 +30,10 @@ int* fault_word_ptr() {
   return g_fault_addr[dev];
 }
 
-gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, float* S,
-                                  cudaStream_t st);
-gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t ldx, double* diag,
-                                cudaStream_t st);
+gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, bool tok_major,
+                                  float* S, cudaStream_t st);
+gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t ldx, bool tok_major,
+                                double* diag, cudaStream_t st);
 size_t prep_workspace_bytes(int64_t d);
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d, int64_t n_seen, float damp,
                              bool desc_act, float* U, int32_t* perm, void* ws, cudaStream_t st);
@@ -133,19 +133,22 @@ using namespace gptq;
 
 extern "C" {
 
-gptq_status_t gptq_hessian_accumulate(const void* X, int64_t d_col, int64_t n_tok, int64_t ldx, float* S,
-                                      double* diag, int64_t* n_seen, gptq_stream_t stream) {
+gptq_status_t gptq_hessian_accumulate(const void* X, int64_t d_col, int64_t n_tok, int64_t ldx,
+                                      int32_t x_token_major, float* S, double* diag, int64_t* n_seen,
+                                      gptq_stream_t stream) {
   if (!X || !S) return GPTQ_ERR_INVALID_ARG;
-  if (d_col < 32 || d_col % 32 != 0 || n_tok < 1 || ldx < n_tok || ldx % 8 != 0)
+  if (x_token_major != 0 && x_token_major != 1) return GPTQ_ERR_INVALID_ARG;
+  const bool tok = x_token_major != 0;
+  if (d_col < 32 || d_col % 32 != 0 || n_tok < 1 || ldx % 8 != 0 || ldx < (tok ? d_col : n_tok))
     return GPTQ_ERR_INVALID_ARG;
   if (d_col > 46336 || n_tok > (int64_t(1) << 28)) return GPTQ_ERR_INVALID_ARG;
   if (!aligned(X, 16) || !aligned(S, 16) || (diag && !aligned(diag, 8))) return GPTQ_ERR_INVALID_ARG;
   if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  gptq_status_t s = launch_hessian_syrk(X, d_col, n_tok, ldx, S, st);
+  gptq_status_t s = launch_hessian_syrk(X, d_col, n_tok, ldx, tok, S, st);
   if (s != GPTQ_OK) return s;
   if (diag) {
-    s = launch_diag_sumsq(X, d_col, n_tok, ldx, diag, st);
+    s = launch_diag_sumsq(X, d_col, n_tok, ldx, tok, diag, st);
     if (s != GPTQ_OK) return s;
   }
   if (n_seen) *n_seen += n_tok;

@@ -13,6 +13,11 @@
 //   * Operands are staged by TMA (128-byte swizzle, 64 tokens per stage)
 //     through a 4-stage mbarrier ring; one thread issues tcgen05.mma, one
 //     thread issues TMA, eight warps drain the accumulators.
+//   * X may be channel-major ([d, n_tok], tokens contiguous: K-major
+//     operands, one box of 128 or 256 channels x 64 tokens per operand) or
+//     token-major ([n_tok, d], channels contiguous: MN-major operands, boxes
+//     of 64 channels x 64 tokens, two for A and four for B, which the MMA
+//     reads through MN-major descriptors).  Same tiles, same schedule.
 //   * Two 256-column TMEM accumulators (all 512 columns).  The tensor cores
 //     add into an accumulator with a rounding that is biased over long
 //     chains (measured: S_ii 0.15% low after 262144 tokens), so one
@@ -92,6 +97,11 @@ __device__ __forceinline__ void job_of(const SyrkSchedule& s, int job, int& ti, 
   tile_of(tile, s.n_i, ti, tj);
 }
 
+// Token-major boxes: 64 channels (128 bytes) x BK tokens = 8 KB each.
+constexpr int TM_BOX = 64;
+constexpr int TM_BOX_BYTES = TM_BOX * BK * 2;
+
+template <bool TOKMAJOR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     hessian_syrk_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_b, SyrkSchedule s, float* __restrict__ S,
@@ -152,8 +162,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &tm_a, full_bar(stage), kb * BK, ti * BM);
-          tma_load_2d(sa + A_BYTES, &tm_b, full_bar(stage), kb * BK, tj * BN);
+          if constexpr (TOKMAJOR) {
+#pragma unroll
+            for (int c = 0; c < BM / TM_BOX; ++c)
+              tma_load_2d(sa + c * TM_BOX_BYTES, &tm_a, full_bar(stage), ti * BM + c * TM_BOX, kb * BK);
+#pragma unroll
+            for (int c = 0; c < BN / TM_BOX; ++c)
+              tma_load_2d(sa + A_BYTES + c * TM_BOX_BYTES, &tm_b, full_bar(stage), tj * BN + c * TM_BOX,
+                          kb * BK);
+          } else {
+            tma_load_2d(sa, &tm_a, full_bar(stage), kb * BK, ti * BM);
+            tma_load_2d(sa + A_BYTES, &tm_b, full_bar(stage), kb * BK, tj * BN);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -164,7 +184,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(BM, BN, /*a f16*/ 0, /*b f16*/ 0);
+      constexpr uint32_t idesc = make_idesc(BM, BN, /*a f16*/ 0, /*b f16*/ 0, TOKMAJOR ? 1 : 0,
+                                            TOKMAJOR ? 1 : 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -188,12 +209,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-            const uint64_t da = smem_desc_sw128_kmajor(sa);
-            const uint64_t db = smem_desc_sw128_kmajor(sa + A_BYTES);
+            uint64_t da, db;
+            if constexpr (TOKMAJOR) {
+              // 64-channel chunks 8 KB apart, 8-token groups 1 KB apart.
+              da = smem_desc_sw128_mnmajor(sa, TM_BOX_BYTES, 1024);
+              db = smem_desc_sw128_mnmajor(sa + A_BYTES, TM_BOX_BYTES, 1024);
+            } else {
+              da = smem_desc_sw128_kmajor(sa);
+              db = smem_desc_sw128_kmajor(sa + A_BYTES);
+            }
 #pragma unroll
             for (int k = 0; k < BK / UK; ++k) {
-              // Advance 32 bytes (16 fp16) along K inside the swizzle atom.
-              const uint64_t off = static_cast<uint64_t>((k * UK * 2) >> 4);
+              // K-major: advance 32 bytes (16 fp16) along K inside the swizzle
+              // atom; MN-major: advance two 8-token groups (2 KB).
+              const uint64_t off =
+                  static_cast<uint64_t>(TOKMAJOR ? (k * UK * 128) >> 4 : (k * UK * 2) >> 4);
               tc_mma_f16(d_tmem, da + off, db + off, idesc, (kb > c0 || k > 0) ? 1u : 0u);
             }
             tc_commit(empty_bar(stage));  // frees the slot when these MMAs finish
@@ -298,12 +328,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_x_map(CUtensorMap* m, const void* X, int64_t d, int64_t n_tok, int64_t ldx, int box_rows) {
+bool make_x_map(CUtensorMap* m, const void* X, int64_t d, int64_t n_tok, int64_t ldx, int box_rows,
+                bool tok_major) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(n_tok), static_cast<cuuint64_t>(d)};
+  // channel-major: [d rows][n_tok]; token-major: [n_tok rows][d], box 64 x BK
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(tok_major ? d : n_tok),
+                        static_cast<cuuint64_t>(tok_major ? n_tok : d)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
-  cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {tok_major ? static_cast<cuuint32_t>(TM_BOX) : static_cast<cuuint32_t>(BK),
+                       tok_major ? static_cast<cuuint32_t>(BK) : static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -344,21 +378,26 @@ static SyrkSchedule make_schedule(int64_t d, int64_t n_tok, int grid_max) {
   return s;
 }
 
-gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, float* S,
-                                  cudaStream_t st) {
+gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64_t ldx, bool tok_major,
+                                  float* S, cudaStream_t st) {
   CUtensorMap tm_a, tm_b;
-  if (!make_x_map(&tm_a, X, d, n_tok, ldx, BM) || !make_x_map(&tm_b, X, d, n_tok, ldx, BN))
+  if (!make_x_map(&tm_a, X, d, n_tok, ldx, BM, tok_major) ||
+      !make_x_map(&tm_b, X, d, n_tok, ldx, BN, tok_major))
     return GPTQ_ERR_CUDA;
+  int* fault = fault_word_ptr();
+  if (!fault) return GPTQ_ERR_CUDA;
   const int sms = sm_count();
   SyrkSchedule s = make_schedule(d, n_tok, sms);
-  static bool attr_set = false;
-  if (!attr_set) {
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(hessian_syrk_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-    attr_set = true;
+  auto kern = tok_major ? hessian_syrk_kernel<true> : hessian_syrk_kernel<false>;
+  static int attr_dev[2] = {-1, -1};   // the attribute is set once per device and layout
+  int dev = 0;
+  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (attr_dev[tok_major ? 1 : 0] != dev) {
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    attr_dev[tok_major ? 1 : 0] = dev;
   }
   const int grid = std::min(sms, s.jobs);
-  hessian_syrk_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, s, S, fault_word_ptr());
+  kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, s, S, fault);
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }

@@ -70,14 +70,25 @@ def cfg_c(**kw):
                                              (64, 64, 60), (64, 100, 100)])
 def test_accumulate_rejects_bad_sizes(lib, d_col, n_tok, ldx):
     n = ctypes.c_int64(0)
-    assert lib.gptq_hessian_accumulate(FAKE, d_col, n_tok, ldx, FAKE, None, ctypes.byref(n),
+    assert lib.gptq_hessian_accumulate(FAKE, d_col, n_tok, ldx, 0, FAKE, None, ctypes.byref(n),
                                        None) == 1
     assert n.value == 0
 
 
 def test_accumulate_rejects_null_and_misaligned(lib):
-    assert lib.gptq_hessian_accumulate(None, 64, 64, 64, FAKE, None, None, None) == 1
-    assert lib.gptq_hessian_accumulate(FAKE + 2, 64, 64, 64, FAKE, None, None, None) == 1
+    assert lib.gptq_hessian_accumulate(None, 64, 64, 64, 0, FAKE, None, None, None) == 1
+    assert lib.gptq_hessian_accumulate(FAKE + 2, 64, 64, 64, 0, FAKE, None, None, None) == 1
+
+
+@pytest.mark.parametrize("d_col,n_tok,ldx,layout", [(64, 100, 56, 1), (64, 100, 60, 1), (64, 40, 64, 2),
+                                                    (96, 10, 72, 1), (64, 100, 64, -1)])
+def test_accumulate_rejects_bad_token_major_args(lib, d_col, n_tok, ldx, layout):
+    """Token-major X [n_tok, d_col] needs ldx >= d_col (a multiple of 8); the
+    layout flag is 0 or 1."""
+    n = ctypes.c_int64(0)
+    assert lib.gptq_hessian_accumulate(FAKE, d_col, n_tok, ldx, layout, FAKE, None, ctypes.byref(n),
+                                       None) == 1
+    assert n.value == 0
 
 
 @pytest.mark.parametrize("kw", [dict(bits=5), dict(bits=1), dict(group_size=48),

@@ -52,6 +52,30 @@ def test_hessian_matches_exact(d_col, n_tok):
     np.testing.assert_allclose(diag.cpu().numpy(), np.diag(S64), rtol=1e-12)
 
 
+@pytest.mark.parametrize("d_col,n_tok,pad", [(512, 2048, 0), (544, 2088, 8), (96, 777, 0),
+                                             (1056, 8200, 24)])
+def test_hessian_token_major_matches_exact(d_col, n_tok, pad):
+    """X given token-major ([n_tok, d_col], channels contiguous, optional
+    row padding): MN-major operand tiles, including channel blocks that run
+    past d_col and a ragged last token slab."""
+    import torch
+    from post_weight_quantization_31_b300 import api
+    X = wl.make_activations(d_col, n_tok, seed=d_col + 3 * n_tok, n_outliers=3, outlier_scale=20.0)
+    Xt = torch.zeros((n_tok, d_col + pad), dtype=torch.float16, device="cuda")
+    Xt[:, :d_col] = torch.from_numpy(np.ascontiguousarray(X.T)).cuda()
+    S = torch.zeros((d_col, d_col), dtype=torch.float32, device="cuda")
+    diag = torch.zeros(d_col, dtype=torch.float64, device="cuda")
+    n = api.hessian_accumulate(Xt[:, :d_col], S, diag, token_major=True)
+    assert n == n_tok
+    S64 = O.hessian_sum(X)
+    assert P.s_error(S.cpu().numpy(), S64) < P.s_tol(n_tok)
+    np.testing.assert_allclose(diag.cpu().numpy(), np.diag(S64), rtol=1e-12)
+    # the two layouts give the same S up to the order of fp32 additions
+    S2 = torch.zeros_like(S)
+    api.hessian_accumulate(torch.from_numpy(X).cuda(), S2)
+    assert P.s_error(S2.cpu().numpy(), S.cpu().numpy().astype(np.float64)) < 2 * P.s_tol(n_tok)
+
+
 def test_hessian_accumulates_over_chunks_and_strides():
     import torch
     from post_weight_quantization_31_b300 import api
