@@ -360,6 +360,101 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
     return line
 
 
+class _OneRank:
+    """torch.distributed stand-in for a single process (collectives are no-ops)."""
+
+    class ReduceOp:
+        SUM = "sum"
+
+    @staticmethod
+    def all_reduce(t, op=None, group=None):
+        return None
+
+    @staticmethod
+    def broadcast(t, src=0, group=None):
+        return None
+
+
+def run_sharded(args, rank: int, world: int, local_rank: int) -> dict | None:
+    """--shard: ONE layer of the benchmark workload solved by all ranks
+    together (strong scaling): each rank accumulates the Hessian of its
+    share of the tokens, one NCCL all-reduce sums S, rank 0 prepares U and
+    broadcasts it with the order, and each rank quantizes and packs its own
+    rows.  A step is one whole layer; the time is the max over ranks."""
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib, sharding
+    build_lib.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    else:
+        dist = _OneRank()
+    inp = make_inputs()
+    cfg = inp.cfg
+    t0, t1 = sharding.token_range(N_TOK, world, rank)
+    r0, r1 = sharding.row_range(D, world, rank)
+    X_local = torch.from_numpy(np.ascontiguousarray(inp.X[:, t0:t1])).to(dev)
+    W_rows = torch.from_numpy(inp.W[r0:r1]).to(torch.bfloat16).to(dev)
+    S = torch.zeros((D, D), dtype=torch.float32, device=dev)
+    U = torch.empty((D, D), dtype=torch.float32, device=dev)
+    perm = torch.empty(D, dtype=torch.int32, device=dev)
+    ws_prep = torch.empty(api.prepare_workspace_size(D), dtype=torch.uint8, device=dev)
+    ws_q = torch.empty(api.quantize_workspace_size(r1 - r0, D, cfg), dtype=torch.uint8, device=dev)
+    out = {}
+
+    def prepare(S_, diag_, n, U_, perm_):
+        api.prepare_hinv(S_, n, cfg, diag=diag_, U=U_, perm=perm_, ws=ws_prep, check=False)
+
+    def quantize(Wr, U_, perm_):
+        api.quantize_layer(Wr, U_, perm_, cfg, out=out, ws=ws_q, check=False)
+        return api.pack(out["codes"], out["zeros"], cfg.bits, cfg.group_size)
+
+    def step():
+        S.zero_()
+        sharding.sharded_layer_solve(dist, rank, X_local=X_local, W_rows=W_rows, rows=(r0, r1), S=S,
+                                     diag=None, U=U, perm=perm,
+                                     accumulate=lambda Xl, S_, d_: api.hessian_accumulate(Xl, S_, d_),
+                                     prepare=prepare, quantize=quantize)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        clk.mark("start")
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark("end")
+    if rank == 0:
+        api.workspace_status(ws_prep, "gptq_prepare_hinv")
+    api.workspace_status(ws_q, "gptq_quantize_layer")
+    ms = max_over_ranks(a.elapsed_time(b), dist if world > 1 else None, dev)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    return {"metric": METRIC, "value": round(D * D * args.steps / (ms * 1e-3) / 1e6, 3),
+            "unit": "Mweights/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "fp16 x fp16 -> fp32 (Hessian), fp32 (solve)",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "d_row": D, "d_col": D, "n_tok": N_TOK,
+                       "l2": "inputs larger than L2 (X is 2.15 GB)",
+                       "parallelism": f"one layer: tokens and rows sharded over {world} GPU(s), "
+                                      "all-reduce of S, broadcast of U"},
+            "clocks": clk.summary()}
+
+
 def measure_dequant(solver, cfg, stream, peaks: dict, reps: int) -> dict:
     """gptq_dequantize of the solved layer's packed output to fp16."""
     import torch
@@ -751,6 +846,9 @@ def main() -> None:
                     help="time only the fused dequant-GEMM for these sizes")
     ap.add_argument("--dqgemm-compare", action="store_true",
                     help="with --dqgemm-only: also time cuBLAS on the dense fp16 weights")
+    ap.add_argument("--shard", action="store_true",
+                    help="solve one layer with all ranks together: token-sharded Hessian + "
+                         "all-reduce, U broadcast, row-sharded quantize (strong scaling)")
     ap.add_argument("--quick-cpu", action="store_true", help="smaller oracle sample")
     ap.add_argument("--syrk-traffic", type=float, default=None,
                     help="DRAM bytes per Hessian launch from an ncu capture")
@@ -771,6 +869,8 @@ def main() -> None:
         line = run_sweep(args)
     elif args.layer_set:
         line = run_layer_set(args)
+    elif args.shard and args.impl == "ours":
+        line = run_sharded(args, rank, world, local_rank)
     elif args.impl == "reference":
         line = run_reference(args, rank)
     else:
