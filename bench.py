@@ -47,10 +47,10 @@ WORKLOAD = ("7B attention projection: W bf16 4096x4096 N(0,0.02^2); X fp16 4096x
 
 
 # DRAM bytes (read + write) of one hessian_syrk_kernel launch at the full
-# workload, from the one-pass ncu capture summarised in
-# profiles/hessian_syrk_dram_4096x262144tok.md.  It describes the kernel
-# source it was measured on (sha256 prefixes below); once that source
-# changes the figure no longer applies and the bench reports null.
+# workload, from a one-pass ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum).  It describes the kernel source it was measured on
+# (sha256 prefixes below); once that source changes the figure no longer
+# applies and the bench reports null.
 SYRK_TRAFFIC = {"bytes": 8.466e9, "n_tok": 262144,
                 "sha256": {"hessian_syrk.cu": "9b0738add5013aeb", "common.cuh": "0ee3a6d05cd5b784"}}
 
@@ -167,42 +167,128 @@ def job_throughput(units_per_rank: float, steps: int, world: int, seconds: float
     return world * units_per_rank * steps / seconds
 
 
-# ---------------------------------------------------------------- inputs
-def fp32_alu_peak_tflops(sms: int = 148, clock_ghz: float = 2.032) -> float:
-    """FP32 FFMA peak: SMs x 128 lanes x 2 flop x the maximum SM clock."""
-    return sms * 128 * 2 * clock_ghz * 1e9 / 1e12
+# ---------------------------------------------------------------- peaks
+def measure_box_peaks(dev) -> dict:
+    """Dense GEMM rates of the types the solve uses, measured here with
+    cuBLAS (torch.matmul, 8192^3, best of 5 after warm-up, CUDA events):
+    TF32 (fp32 inputs with TF32 allowed) and FP32 (TF32 off).  3xTF32 does
+    three TF32 products per output term, so its peak is TF32 / 3."""
+    import torch
+    n = 8192
+    a = torch.randn((n, n), device=dev)
+    b = torch.randn((n, n), device=dev)
+    out = {}
+    old = torch.backends.cuda.matmul.allow_tf32
+    try:
+        for name, tf32 in (("tf32_tflops", True), ("fp32_tflops", False)):
+            torch.backends.cuda.matmul.allow_tf32 = tf32
+            for _ in range(2):
+                torch.matmul(a, b)
+            best = float("inf")
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch.matmul(a, b)
+                e1.record()
+                torch.cuda.synchronize(dev)
+                best = min(best, e0.elapsed_time(e1))
+            out[name] = round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+    out["tf32x3_tflops"] = round(out["tf32_tflops"] / 3.0, 1)
+    out["how"] = "cuBLAS via torch.matmul 8192^3, best of 5 (CUDA events), this run"
+    return out
+
+
+def prepare_gemm_ms(d: int, dev, reps: int = 3) -> float:
+    """Time of the prepare step's update GEMMs alone: the same 3xTF32
+    launches (M = d - k - 128 rows, N = d lower, K = 128, for every step k)
+    replayed through the library's GEMM on synthetic operands, CUDA events
+    around all of them, best of `reps`.  The prepare time minus this is the
+    panel (factorization) share."""
+    import ctypes
+
+    import torch
+    from post_weight_quantization_31_b300 import _lib
+    lib = _lib.load()
+    f = lib.gptq_internal_tgemm
+    f.restype = ctypes.c_int
+    vp, i64, i32, fl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32, i32, fl, fl, vp, i64, i32, i32, i32, vp]
+    nb = 128
+    Bh = torch.randn((d, nb), device=dev) * 1e-3
+    Bl = torch.zeros_like(Bh)
+    Z = torch.zeros((d, d), device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    best = float("inf")
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(0, d - nb, nb):
+            r = k + nb
+            rc = f(Bh[r:].data_ptr(), Bl[r:].data_ptr(), nb, Bh.data_ptr(), Bl.data_ptr(), nb, d - r, d, nb,
+                   -1.0, 1.0, Z[r:].data_ptr(), d, 1, r, 0, st)
+            if rc != 0:
+                raise RuntimeError(f"gptq_internal_tgemm failed: {rc}")
+        e1.record()
+        torch.cuda.synchronize(dev)
+        best = min(best, e0.elapsed_time(e1))
+    return best
+
+
+def prepare_gemm_flops(d: int, nb: int = 128) -> float:
+    """Flops of those update GEMMs: for step k, rows r >= k + nb, columns
+    c <= r (lower), K = nb, 2 flops per multiply-add."""
+    tot = 0.0
+    for k in range(0, d - nb, nb):
+        r = k + nb
+        rows = d - r
+        # sum over rows i in [r, d) of (i + 1) columns
+        tot += 2.0 * nb * (rows * (r + d + 1) / 2.0)
+    return tot
 
 
 def phase_rooflines(ph_ms: dict, d_row: int, d_col: int, bits: int, group_size: int,
-                    peaks: dict, block: int = 128) -> dict:
+                    peaks: dict, box: dict | None = None, prep_gemm_ms: float | None = None,
+                    block: int = 128) -> dict:
     """Roofline fraction of each solve phase from its CUDA-event time and its
-    algorithmic work:
-      prepare   2·d³/3 flop (the reverse-route Cholesky with its inverse)
-                against the FP32 FFMA peak (the panels are FP32 ALU work; the
-                trailing updates run as 3xTF32 on the tensor cores);
+    algorithmic work, each against the measured peak of the unit it runs on:
+      prepare   its update GEMMs (3xTF32 on the tensor cores) against the
+                measured 3xTF32 rate, over their own replayed time; the rest
+                of the phase (the panel factorizations, a latency chain) is
+                reported as time only;
       quantize  the trailing updates' d_row·d_col·(d_col − B) flop against
-                the 3xTF32 rate (a third of the TF32 peak, TF32 = bf16 / 2
-                nominal); the column loop inside the same phase moves
-                read W (2 B) + codes (bits/8 B) + scale/zero (5 B per group
-                element) per weight, reported against HBM;
+                the 3xTF32 rate, over the phase time; the column loop inside
+                the same phase moves read W (2 B) + codes (bits/8 B) +
+                scale/zero (5 B per group element) per weight, reported
+                against HBM;
       pack      1 + bits/8 B per weight against HBM."""
     hbm = float(peaks.get("hbm_gbs", 6400.0))
-    tf32_3x = float(peaks.get("bf16_tflops", 1800.0)) / 2.0 / 3.0
-    alu = fp32_alu_peak_tflops()
+    if box:
+        tf32_3x, src = float(box["tf32x3_tflops"]), "measured cuBLAS TF32 / 3"
+    else:
+        tf32_3x, src = float(peaks.get("bf16_tflops", 1800.0)) / 2.0 / 3.0, "nominal (bf16 / 2 / 3)"
     W = float(d_row) * d_col
     G = 1 if group_size == -1 else d_col // group_size
     out = {}
     t = ph_ms.get("prepare")
     if t:
-        a = 2.0 * d_col ** 3 / 3.0 / (t * 1e-3) / 1e12
-        out["prepare"] = {"bound": "alu", "achieved": round(a, 2), "peak": round(alu, 1),
-                          "unit": "TFLOP/s", "frac": round(a / alu, 4)}
+        entry = {"ms": round(t, 4)}
+        if prep_gemm_ms:
+            fl = prepare_gemm_flops(d_col)
+            a = fl / (prep_gemm_ms * 1e-3) / 1e12
+            entry.update({"gemm": {"bound": "tensor", "ms": round(prep_gemm_ms, 4), "flop": fl,
+                                   "achieved": round(a, 1), "peak": tf32_3x, "unit": "TFLOP/s",
+                                   "frac": round(a / tf32_3x, 4)},
+                          "panel_ms": round(max(t - prep_gemm_ms, 0.0), 4),
+                          "panel_note": "diagonal-block factorizations: a latency chain, time only"})
+        out["prepare"] = entry
     t = ph_ms.get("quantize")
     if t:
         a = W * max(d_col - block, 0) / (t * 1e-3) / 1e12
         col_bytes = W * (2.0 + bits / 8.0) + 5.0 * G * d_row
         b = col_bytes / (t * 1e-3) / 1e9
-        out["quantize"] = {"bound": "tensor", "achieved": round(a, 2), "peak": round(tf32_3x, 1),
+        out["quantize"] = {"bound": "tensor", "achieved": round(a, 2), "peak": tf32_3x,
                            "unit": "TFLOP/s", "frac": round(a / tf32_3x, 4),
                            "column_loop_bytes": int(col_bytes), "column_loop_gbs": round(b, 1),
                            "column_loop_frac_of_hbm": round(b / hbm, 4)}
@@ -211,8 +297,7 @@ def phase_rooflines(ph_ms: dict, d_row: int, d_col: int, bits: int, group_size: 
         b = W * (1.0 + bits / 8.0) / (t * 1e-3) / 1e9
         out["pack"] = {"bound": "hbm", "achieved": round(b, 1), "peak": hbm, "unit": "GB/s",
                        "frac": round(b / hbm, 4)}
-    out["peak_note"] = (f"{peaks.get('source', 'fallback')} HBM and bf16 burst; TF32 = bf16/2 and FP32 "
-                        f"FFMA = 148 x 128 x 2 x 2.032 GHz, both nominal")
+    out["peak_note"] = (f"HBM: {peaks.get('source', 'fallback')} copy bandwidth; 3xTF32: {src}")
     return out
 
 
@@ -314,15 +399,25 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
             dist.destroy_process_group()
         return None
 
+    box = measure_box_peaks(dev)
+    prep_gemm = prepare_gemm_ms(D, dev)
     peaks = measured_peaks()
     syrk_ms = ph["hessian"]
     flops = float(N_TOK) * D * (D + 1)       # symmetric half of X X^T
     achieved = flops / (syrk_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", 1400.0))
+    # The kernel is timed inside a 7 ms step, not a seconds-long loop, and the
+    # step's clock samples sit at the maximum SM clock: the burst peak is the
+    # denominator; the sustained (power-capped) one is given beside it.
+    peak = float(peaks.get("bf16_tflops", 1800.0))
+    sus = float(peaks.get("bf16_tflops_sustained", 1400.0))
+    clocks = clk.summary()
     roof = {"kernel": "hessian_syrk_kernel (tcgen05 kind::f16, fp16 x fp16 -> fp32)",
             "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
-            "peak_note": f"{peaks['source']} bf16 dense sustained (fp16 rate = bf16 rate)",
+            "frac_of_sustained": round(achieved / sus, 4),
+            "peak_note": (f"{peaks['source']} bf16 dense burst {peak} TFLOP/s (fp16 rate = bf16 rate), "
+                          f"SM clock in the timed region {clocks.get('sm_mhz')} MHz; sustained "
+                          f"{sus} TFLOP/s was measured at {peaks.get('clocks_under_load', {}).get('sm_mhz_median')} MHz"),
             "traffic": args.syrk_traffic if args.syrk_traffic is not None else syrk_traffic(),
             "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
     ms_step = elapsed_ms / args.steps
@@ -338,13 +433,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> dict | None:
                    "l2": "inputs larger than L2 (X is 2.15 GB)",
                    "parallelism": f"one independent layer per GPU x{world}"},
         "phases_ms": {k: round(v, 4) for k, v in ph.items()},
-        "phases_roofline": phase_rooflines(ph, D, D, cfg.bits, cfg.group_size, peaks),
+        "phases_roofline": phase_rooflines(ph, D, D, cfg.bits, cfg.group_size, peaks, box=box,
+                                           prep_gemm_ms=prep_gemm),
+        "box_peaks": box,
         "solve_only": {"value": round(D * D / ((ph["prepare"] + ph["quantize"] + ph["pack"]) * 1e-3) / 1e6, 3),
                        "unit": "Mweights/s",
                        "note": "prepare + quantize + pack with H given, from the same timed steps"},
         "gpu_launches": int(launches),
         "roofline": roof,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": e2e,
     }
     if args.dequant_reps > 0:

@@ -50,16 +50,35 @@ def test_single_rank_is_identity():
 
 def test_phase_rooflines_scale_with_time():
     """Achieved rates are work / time: halving a phase's time doubles its
-    rate; fractions are achieved / peak with the stated peaks."""
+    rate; fractions are achieved / peak with the stated peaks; the prepare
+    step's GEMM share is quoted against the measured 3xTF32 rate."""
     import bench
     peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0, "source": "test"}
+    box = {"tf32_tflops": 900.0, "tf32x3_tflops": 300.0, "fp32_tflops": 70.0}
     ph = {"prepare": 2.0, "quantize": 1.0, "pack": 0.1}
-    a = bench.phase_rooflines(ph, 4096, 4096, 4, 128, peaks)
-    b = bench.phase_rooflines({k: v / 2 for k, v in ph.items()}, 4096, 4096, 4, 128, peaks)
-    for k in ("prepare", "quantize", "pack"):
+    a = bench.phase_rooflines(ph, 4096, 4096, 4, 128, peaks, box=box, prep_gemm_ms=0.5)
+    b = bench.phase_rooflines({k: v / 2 for k, v in ph.items()}, 4096, 4096, 4, 128, peaks, box=box,
+                              prep_gemm_ms=0.25)
+    for k in ("quantize", "pack"):
         assert abs(b[k]["achieved"] / a[k]["achieved"] - 2.0) < 1e-3
         assert abs(a[k]["frac"] - a[k]["achieved"] / a[k]["peak"]) < 1e-3
-    # prepare: 2/3 d^3 flop in 2 ms; pack: 1.5 B/weight in 0.1 ms
-    assert abs(a["prepare"]["achieved"] - 2 * 4096 ** 3 / 3 / 2e-3 / 1e12) < 0.01
+    g = a["prepare"]["gemm"]
+    assert abs(b["prepare"]["gemm"]["achieved"] / g["achieved"] - 2.0) < 2e-3
+    assert g["peak"] == 300.0 and abs(g["frac"] - g["achieved"] / 300.0) < 1e-3
+    assert abs(a["prepare"]["panel_ms"] - 1.5) < 1e-9
+    # pack: 1.5 B/weight in 0.1 ms; quantize against the measured 3xTF32 rate
     assert abs(a["pack"]["achieved"] - 4096 * 4096 * 1.5 / 1e-4 / 1e9) < 0.1
-    assert a["quantize"]["peak"] == round(1800.0 / 2 / 3, 1)
+    assert a["quantize"]["peak"] == 300.0
+
+
+def test_prepare_gemm_flops_is_the_lower_triangle_count():
+    """Replayed update GEMM flops: brute-force count of the lower-triangle
+    elements each step updates, 2 * K flops each; about 2 d^3 / 3 in all."""
+    import bench
+    d, nb = 512, 128
+    want = 0
+    for k in range(0, d - nb, nb):
+        for i in range(k + nb, d):
+            want += 2 * nb * (i + 1)
+    assert bench.prepare_gemm_flops(d, nb) == want
+    assert abs(bench.prepare_gemm_flops(4096) / (2 * 4096 ** 3 / 3) - 1) < 0.05
