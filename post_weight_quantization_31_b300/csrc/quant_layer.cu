@@ -101,11 +101,6 @@ __device__ __forceinline__ QParams grid_params(float xmin, float xmax, float max
   return grid_from_span(xmax - xmin, -xmin, maxq, 0);
 }
 
-// clamp(rint(w / s) + z, 0, maxq) as a float.
-__device__ __forceinline__ float grid_code(float w, const QParams& p, float maxq) {
-  return fminf(fmaxf(rintf(maxq * div_span(w, p)) + p.z, 0.f), maxq);
-}
-
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>
@@ -189,7 +184,7 @@ struct ColumnArgs {
   const float* row_span;  // group_size = -1: span of each row's grid
 };
 
-__global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) {
+__global__ void __launch_bounds__(CL_THREADS, 2) column_block_kernel(ColumnArgs a) {
   extern __shared__ __align__(16) float smem[];
   float* Us = smem;                                  // [CB][UROW]
   float* inv_d = Us + CB * UROW;                     // [CB]
@@ -248,6 +243,13 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
 #pragma unroll
   for (int k = 0; k < CPL; ++k) e_own[k] = q_own[k] = 0.f;
   const int src_base = lane & ~(LPR - 1);
+  // Every lane carries the value of the column being quantized (v) and of
+  // the next column as it stood before the current column's update (nx):
+  // v_{j+1} = nx - e_j U[j][j+1] is one FMA after e_j (the same FMA the
+  // owner lane does), so the shuffle that fetches the following nx from
+  // its owner runs beside the next decision instead of in front of it.
+  float v = __shfl_sync(0xffffffffu, w[0], src_base);
+  float nx = __shfl_sync(0xffffffffu, w[1], src_base);
   for (int seg = 0; seg < nc / CPL; ++seg) {
     const int seg_start = i1 + CPL * seg;
     const bool gstart = a.gs > 0 && (seg_start % a.gs) == 0;
@@ -277,10 +279,12 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
         }
       }
       const int j = CPL * seg + k;
-      const float v = __shfl_sync(0xffffffffu, w[k], src_base | seg);
-      const float q = grid_code(v, p, a.maxq);
-      const float dq = p.s * (q - p.z);
-      const float e = (v - dq) * inv_d[j];
+      // code - z = clamp(rint(v / s), -z, maxq - z); dq = s (code - z)
+      const float qz = fminf(fmaxf(rintf(a.maxq * div_span(v, p)), -p.z), a.maxq - p.z);
+      const float e = (v - p.s * qz) * inv_d[j];
+      const int jn = (j + 1) & (CB - 1);
+      const float u_next = Us[j * UROW + (jn / CPL) * USEG + (jn % CPL)];
+      v = fmaf(-e, u_next, nx);
       const float* urow = urow_base + k * UROW;
 #pragma unroll
       for (int t = 0; t < CPL; t += 4) {
@@ -290,12 +294,14 @@ __global__ void __launch_bounds__(CL_THREADS) column_block_kernel(ColumnArgs a) 
         w[t + 2] = fmaf(-e, u4.z, w[t + 2]);
         w[t + 3] = fmaf(-e, u4.w, w[t + 3]);
       }
+      // nx for column j+1: column j+2 after column j's update, from its owner
+      nx = __shfl_sync(0xffffffffu, w[(k + 2) % CPL], src_base | ((seg + (k + 2) / CPL) % LPR));
       // The owner lane keeps the error and code of its own columns in
       // registers (no shared-memory stores inside the loop, so the next
       // columns' U loads can be issued early).
       if (sub == seg) {
         e_own[k] = e;
-        q_own[k] = q;
+        q_own[k] = qz + p.z;
       }
     }
   }
