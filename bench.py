@@ -714,6 +714,82 @@ def run_layer_set(args) -> dict:
             "config": {"workload": r["workload"], "layers_timed": r["layers_timed"]}, **r}
 
 
+def run_awq(args) -> dict:
+    """--awq: the AWQ scale search on the benchmark layer (4-bit g128, the 13
+    candidates 1, 1.25, ..., 4, 5% salient channels).  A step: S = 0,
+    accumulate (with the fp64 channel sums of squares the statistic needs),
+    search (13 x: RTN of W diag(t), E = D S on the tensor cores, sum E .* D;
+    then the choice and the final RTN on the device), pack.  Roofline: the
+    search's GEMM flops (13 x 2 d_row d_col^2, useful products) against the
+    measured 3xTF32 rate."""
+    import torch
+    from post_weight_quantization_31_b300 import api, build_lib
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    inp = make_inputs()
+    cfg = inp.cfg
+    X = torch.from_numpy(inp.X).to(dev)
+    W = torch.from_numpy(inp.W).to(torch.bfloat16).to(dev)
+    S = torch.zeros((D, D), dtype=torch.float32, device=dev)
+    diag = torch.zeros(D, dtype=torch.float64, device=dev)
+    grid = api.AWQ_GRID
+    ws = torch.empty(int(api._lib.load().gptq_awq_workspace_size(D, D, len(grid))), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None):
+        S.zero_()
+        diag.zero_()
+        if e:
+            e[0].record(stream)
+        api.hessian_accumulate(X, S, diag)
+        if e:
+            e[1].record(stream)
+        out = api.awq_search(W, S, diag, cfg, grid=grid, ws=ws, check=False)
+        if e:
+            e[2].record(stream)
+        api.pack(out["codes"], out["zeros"], cfg.bits, cfg.group_size)
+        if e:
+            e[3].record(stream)
+        return out
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(0) as clk:
+        clk.mark("start")
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            out = step(ev[k])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        clk.mark("end")
+    api.workspace_status(ws, "gptq_awq_search")
+    ms = t0.elapsed_time(t1) / args.steps
+    search_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    box = measure_box_peaks(dev)
+    fl = len(grid) * 2.0 * D * D * D
+    a = fl / (search_ms * 1e-3) / 1e12
+    return {"metric": "AWQ layer search Mweights/s (4096x4096, 4-bit g128, 13 candidates)",
+            "value": round(D * D / (ms * 1e-3) / 1e6, 3), "unit": "Mweights/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "dtype": "fp16 x fp16 -> fp32 (Hessian), 3xTF32 / fp64 (errors)",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD.replace("desc_act off", "AWQ, 5% salient channels"),
+                       "l2": "inputs larger than L2 (X is 2.15 GB)"},
+            "phases_ms": {"hessian": round(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), 4),
+                          "search": round(search_ms, 4),
+                          "pack": round(statistics.mean(e[2].elapsed_time(e[3]) for e in ev), 4)},
+            "roofline": {"kernel": "tgemm_kernel (3xTF32, E = D S per candidate)", "bound": "tensor",
+                         "achieved": round(a, 1), "peak": box["tf32x3_tflops"], "unit": "TFLOP/s",
+                         "frac": round(a / box["tf32x3_tflops"], 4),
+                         "peak_note": "measured cuBLAS TF32 / 3, this run; achieved over the whole search phase"},
+            "chosen_factor": float(out["t"].max().item()),
+            "clocks": clk.summary()}
+
+
 def run_sweep(args) -> dict:
     """--sweep BITS:GS[:act],...: the bench step (S = 0, accumulate, prepare,
     quantize, pack) on the bench workload for other quantizer settings
@@ -943,6 +1019,7 @@ def main() -> None:
                     help="time only the fused dequant-GEMM for these sizes")
     ap.add_argument("--dqgemm-compare", action="store_true",
                     help="with --dqgemm-only: also time cuBLAS on the dense fp16 weights")
+    ap.add_argument("--awq", action="store_true", help="time the AWQ scale search on the benchmark layer")
     ap.add_argument("--shard", action="store_true",
                     help="solve one layer with all ranks together: token-sharded Hessian + "
                          "all-reduce, U broadcast, row-sharded quantize (strong scaling)")
@@ -966,6 +1043,8 @@ def main() -> None:
         line = run_sweep(args)
     elif args.layer_set:
         line = run_layer_set(args)
+    elif args.awq:
+        line = run_awq(args)
     elif args.shard and args.impl == "ours":
         line = run_sharded(args, rank, world, local_rank)
     elif args.impl == "reference":

@@ -268,6 +268,46 @@ GPTQ_API gptq_status_t gptq_unpack(const int32_t* qweight, const int32_t* qzeros
                           int64_t d_col, int32_t bits, int32_t group_size, uint8_t* codes,
                           uint8_t* zeros, gptq_stream_t stream);
 
+/* Bytes of workspace gptq_awq_search needs for d_row x d_col and n_grid
+ * candidate factors. */
+GPTQ_API size_t gptq_awq_workspace_size(int64_t d_row, int64_t d_col, int32_t n_grid);
+
+/*
+ * AWQ scale search, the activation-aware alternative to the GPTQ solve
+ * ("大模型压缩量化技术：GPTQ 与 AWQ 原理详解", §四 AWQ 原理; "GPTQ/AWQ量化导出",
+ * AWQ steps).  The channels whose activations are largest -- the
+ * ceil(salient_frac * d_col) largest RMS sqrt(sum_t x^2 / n), ties to the
+ * lower index -- have their weights multiplied by one factor s before
+ * round-to-nearest quantization (the GPTQ grid of cfg, group-wise in
+ * natural column order); the effective weights are the dequantized values
+ * divided by s, and at inference those activations are divided by s.  s is
+ * the candidate in `grid` with the smallest layer output error
+ * tr(D S D^T), D = W - effective weights (the earliest on ties).
+ *   W        [d_row, d_col] of w_dtype, 16-byte aligned.  Read only.
+ *   S, diag  from gptq_hessian_accumulate over the layer's calibration
+ *            tokens (diag, the fp64 sums of squares, is required).
+ *   cfg      bits, group_size (32, 64, 128 dividing d_col, or -1) and sym;
+ *            the other fields are not used.
+ *   salient_frac  in (0, 1]; 0.05 on the pages.
+ *   grid     HOST array of n_grid (1..256) positive candidate factors, e.g.
+ *            1, 1.25, ..., 4 (1 keeps plain round-to-nearest among them).
+ *   codes    uint8 [d_row, d_col] output: codes of W diag(t), natural order
+ *            (g_idx[c] = c / group_size for gptq_pack's consumers).
+ *   scales   fp32 [G, d_row], zeros uint8 [G, d_row] outputs (of W diag(t)).
+ *   t        fp32 [d_col] output: s for the salient channels, 1 elsewhere.
+ *   errors   fp64 [n_grid] device output (may be NULL): each candidate's
+ *            error tr(D S D^T), with S as given (so in units of X X^T).
+ *   ws       gptq_awq_workspace_size bytes, 256-byte aligned.
+ *   Asynchronous; a wait that runs out lands in the status word of ws
+ *   (gptq_workspace_status).  The error products run on the tensor cores
+ *   (3xTF32, fp32-accurate) and are summed in fp64.
+ */
+GPTQ_API gptq_status_t gptq_awq_search(const void* W, int32_t w_dtype, int64_t d_row, int64_t d_col,
+                                       const float* S, const double* diag, const gptq_config_t* cfg,
+                                       float salient_frac, const float* grid, int32_t n_grid,
+                                       uint8_t* codes, float* scales, uint8_t* zeros, float* t,
+                                       double* errors, void* ws, size_t ws_bytes, gptq_stream_t stream);
+
 /*
  * The packed layer back to dense weights, in the ORIGINAL column order:
  *   W_out[r][c] = scales[g][r] * (code[r][c] - zero[g][r]),  g = g_idx[c],

@@ -46,6 +46,9 @@ SIGNATURES = {
     "gptq_quantize_workspace_size": (_sz, [_i64, _i64, _CFGP]),
     "gptq_quantize_layer": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _CFGP, _vp, _vp, _vp, _vp,
                                    _vp, _sz, _vp]),
+    "gptq_awq_workspace_size": (_sz, [_i64, _i64, _i32]),
+    "gptq_awq_search": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _CFGP, ctypes.c_float, _vp, _i32, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _sz, _vp]),
     "gptq_pack": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp]),
     "gptq_unpack": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp]),
     "gptq_dequantize": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _i32, _vp, _vp]),

@@ -185,6 +185,45 @@ def quantize_layer(W: torch.Tensor, U: torch.Tensor, perm: torch.Tensor, cfg: Qu
     return out
 
 
+# ----------------------------------------------------------------------- AWQ
+AWQ_GRID = tuple(1.0 + 0.25 * i for i in range(13))      # 1, 1.25, ..., 4
+
+
+def awq_search(W: torch.Tensor, S: torch.Tensor, diag: torch.Tensor, cfg: QuantConfig,
+               salient_frac: float = 0.05, grid=AWQ_GRID, ws: torch.Tensor | None = None,
+               check: bool = True) -> dict:
+    """AWQ scale search (see gptq_awq_search in include/gptq.h).  Returns
+    dict(codes uint8 [d_row, d_col] of W diag(t), scales fp32 [G, d_row],
+    zeros uint8 [G, d_row], t fp32 [d_col], errors fp64 [n_grid])."""
+    lib = _lib.load()
+    if W.dtype not in _WDT:
+        raise ValueError("W must be fp32, bf16 or fp16")
+    _contig(W, "W")
+    d_row, d_col = W.shape
+    _need(S, torch.float32, "S", (d_col, d_col))
+    _contig(S, "S")
+    _need(diag, torch.float64, "diag", (d_col,))
+    dev = W.device
+    G = n_groups(cfg.group_size, d_col)
+    g = (ctypes.c_float * len(grid))(*[float(v) for v in grid])
+    out = {"codes": torch.empty((d_row, d_col), dtype=torch.uint8, device=dev),
+           "scales": torch.empty((G, d_row), dtype=torch.float32, device=dev),
+           "zeros": torch.empty((G, d_row), dtype=torch.uint8, device=dev),
+           "t": torch.empty(d_col, dtype=torch.float32, device=dev),
+           "errors": torch.empty(len(grid), dtype=torch.float64, device=dev)}
+    need = int(lib.gptq_awq_workspace_size(d_row, d_col, len(grid)))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if ws is None else ws
+    c = _lib.make_config(cfg)
+    _check(lib.gptq_awq_search(W.data_ptr(), _WDT[W.dtype], d_row, d_col, S.data_ptr(), diag.data_ptr(),
+                               ctypes.byref(c), float(salient_frac), ctypes.cast(g, ctypes.c_void_p),
+                               len(grid), out["codes"].data_ptr(), out["scales"].data_ptr(),
+                               out["zeros"].data_ptr(), out["t"].data_ptr(), out["errors"].data_ptr(),
+                               ws.data_ptr(), ws.numel(), _stream()), "gptq_awq_search")
+    if check:
+        workspace_status(ws, "gptq_awq_search")
+    return out
+
+
 # ----------------------------------------------------------------------- a5
 def pack(codes: torch.Tensor, zeros: torch.Tensor, bits: int, group_size: int,
          qweight: torch.Tensor | None = None, qzeros: torch.Tensor | None = None):

@@ -46,6 +46,11 @@ gptq_status_t launch_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_
                           int bits, int n_groups, int32_t* qweight, int32_t* qzeros, cudaStream_t st);
 gptq_status_t launch_unpack(const int32_t* qweight, const int32_t* qzeros, int64_t d_row, int64_t d_col,
                             int bits, int n_groups, uint8_t* codes, uint8_t* zeros, cudaStream_t st);
+size_t awq_workspace_bytes(int64_t d_row, int64_t d_col, int n_grid);
+gptq_status_t launch_awq(const void* W, int w_dtype, int64_t d_row, int64_t d_col, const float* S,
+                         const double* diag, const gptq_config_t& cfg, float frac, const float* grid_host,
+                         int n_grid, uint8_t* codes, float* scales, uint8_t* zeros, float* t_out,
+                         double* errors_out, void* ws, cudaStream_t st);
 gptq_status_t launch_dequant(const int32_t* qweight, const int32_t* qzeros, const float* scales,
                              const int32_t* g_idx, int64_t d_row, int64_t d_col, int bits, int n_groups,
                              int out_dtype, void* W, cudaStream_t st);
@@ -198,6 +203,36 @@ gptq_status_t gptq_quantize_layer(const void* W, int32_t w_dtype, int64_t d_row,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return launch_quantize(W, w_dtype, d_row, d_col, U, perm, *cfg, codes, scales, zeros, g_idx, ws,
                          st);
+}
+
+size_t gptq_awq_workspace_size(int64_t d_row, int64_t d_col, int32_t n_grid) {
+  if (d_row <= 0 || d_col <= 0 || n_grid <= 0) return 0;
+  return awq_workspace_bytes(d_row, d_col, n_grid);
+}
+
+gptq_status_t gptq_awq_search(const void* W, int32_t w_dtype, int64_t d_row, int64_t d_col, const float* S,
+                              const double* diag, const gptq_config_t* cfg, float salient_frac,
+                              const float* grid, int32_t n_grid, uint8_t* codes, float* scales,
+                              uint8_t* zeros, float* t, double* errors, void* ws, size_t ws_bytes,
+                              gptq_stream_t stream) {
+  if (!W || !S || !diag || !cfg || !grid || !codes || !scales || !zeros || !t) return GPTQ_ERR_INVALID_ARG;
+  if (w_dtype != GPTQ_W_FP32 && w_dtype != GPTQ_W_BF16 && w_dtype != GPTQ_W_FP16) return GPTQ_ERR_INVALID_ARG;
+  if (d_row < 32 || d_row % 32 != 0 || d_col < 32 || d_col % 32 != 0 || d_col > 46336) return GPTQ_ERR_INVALID_ARG;
+  if (d_row * d_col > (int64_t(1) << 31) - 1) return GPTQ_ERR_INVALID_ARG;
+  if (!bits_ok(cfg->bits) || (cfg->sym != 0 && cfg->sym != 1)) return GPTQ_ERR_INVALID_ARG;
+  const int gs = cfg->group_size;
+  if (gs != -1 && (gs <= 0 || gs % 32 != 0 || d_col % gs != 0)) return GPTQ_ERR_INVALID_ARG;
+  if (!(salient_frac > 0.f) || salient_frac > 1.f) return GPTQ_ERR_INVALID_ARG;
+  if (n_grid < 1 || n_grid > 256) return GPTQ_ERR_INVALID_ARG;
+  for (int i = 0; i < n_grid; ++i)
+    if (!(grid[i] > 0.f) || !std::isfinite(grid[i])) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || !aligned(S, 16) || !aligned(diag, 8) || !aligned(scales, 4) || !aligned(t, 4) ||
+      (errors && !aligned(errors, 8)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < awq_workspace_bytes(d_row, d_col, n_grid)) return GPTQ_ERR_WORKSPACE;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  return launch_awq(W, w_dtype, d_row, d_col, S, diag, *cfg, salient_frac, grid, n_grid, codes, scales, zeros,
+                    t, errors, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
 gptq_status_t gptq_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,

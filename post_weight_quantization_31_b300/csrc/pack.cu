@@ -33,16 +33,19 @@ __device__ __forceinline__ uint32_t stream_word(const uint8_t* c, int stride, in
 
 __global__ void pack_qweight_kernel(const uint8_t* __restrict__ codes, int d_row, int d_col, int bits,
                                     int32_t* __restrict__ qweight) {
-  __shared__ __align__(16) uint8_t tile[PK_ROWS][PK_COLS];
+  // Rows padded by one word: the 32 lanes below each read a different row
+  // at the same column, and a 260-byte row stride puts those reads in 32
+  // different banks (an unpadded 256-byte stride would put all of them in one).
+  __shared__ __align__(16) uint8_t tile[PK_ROWS][PK_COLS + 4];
   const int r0 = blockIdx.y * PK_ROWS;
   const int c0 = blockIdx.x * PK_COLS;
   const int ncols = min(PK_COLS, d_col - c0);
-  for (int idx = threadIdx.x; idx < PK_ROWS * (PK_COLS / 16); idx += blockDim.x) {
-    const int rr = idx / (PK_COLS / 16), cc = (idx % (PK_COLS / 16)) * 16;
-    uint4 v = make_uint4(0, 0, 0, 0);
+  for (int idx = threadIdx.x; idx < PK_ROWS * (PK_COLS / 4); idx += blockDim.x) {
+    const int rr = idx / (PK_COLS / 4), cc = (idx % (PK_COLS / 4)) * 4;
+    uint32_t v = 0;
     if (r0 + rr < d_row && cc < ncols)
-      v = *reinterpret_cast<const uint4*>(codes + static_cast<size_t>(r0 + rr) * d_col + c0 + cc);
-    *reinterpret_cast<uint4*>(&tile[rr][cc]) = v;
+      v = *reinterpret_cast<const uint32_t*>(codes + static_cast<size_t>(r0 + rr) * d_col + c0 + cc);
+    *reinterpret_cast<uint32_t*>(&tile[rr][cc]) = v;
   }
   __syncthreads();
   const uint32_t mask = (1u << bits) - 1u;

@@ -206,3 +206,28 @@ def test_dequant_matmul_rejects_bad_args(lib):
     assert call(gi=FAKE + 4) == 1       # g_idx must be 16-byte aligned
     assert call(sc=FAKE + 4) == 1       # scales must be 16-byte aligned
     assert call(Y=0) == 1
+
+
+@pytest.mark.parametrize("kw,frac,grid", [(dict(), 0.0, [1.0]), (dict(), 1.5, [1.0]),
+                                          (dict(), 0.05, []), (dict(), 0.05, [1.0, -2.0]),
+                                          (dict(bits=5), 0.05, [1.0]), (dict(group_size=48), 0.05, [1.0])])
+def test_awq_rejects_bad_args(lib, kw, frac, grid):
+    c = cfg_c(**kw)
+    g = (ctypes.c_float * max(1, len(grid)))(*grid)
+    need = lib.gptq_awq_workspace_size(64, 256, max(1, len(grid)))
+    st = lib.gptq_awq_search(FAKE, 1, 64, 256, FAKE, FAKE, ctypes.byref(c), frac,
+                             ctypes.cast(g, ctypes.c_void_p), len(grid), FAKE, FAKE, FAKE, FAKE, None,
+                             FAKE, need, None)
+    assert st == 1, (kw, frac, grid)
+
+
+def test_awq_rejects_missing_diag_and_small_workspace(lib):
+    c = cfg_c()
+    g = (ctypes.c_float * 2)(1.0, 2.0)
+    need = lib.gptq_awq_workspace_size(64, 256, 2)
+    args = [FAKE, 1, 64, 256, FAKE, None, ctypes.byref(c), 0.05, ctypes.cast(g, ctypes.c_void_p), 2,
+            FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None]
+    assert lib.gptq_awq_search(*args) == 1
+    args[5] = FAKE
+    args[16] = need - 1
+    assert lib.gptq_awq_search(*args) == 4
