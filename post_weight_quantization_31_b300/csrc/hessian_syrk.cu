@@ -25,11 +25,19 @@
 //     add it into fp32 registers with round-to-nearest while the MMAs fill
 //     the other accumulator.  A job's sum leaves the registers once, at its
 //     end.
-//   * Jobs: whole tiles with the full token range first, in waves of one
-//     tile per CTA (every CTA of a wave sweeps the tokens at the same pace,
-//     so each X slab is read from HBM about once per wave and re-served from
-//     L2); the tiles left over after the last full wave are split along the
-//     tokens into `ks` pieces to balance the final wave.
+//   * CTAs run in clusters of two that take the two tiles (ti, tj) and
+//     (ti + 1, tj) of one column block: they share the tile's 256 B rows,
+//     so each CTA loads its own A and one half of B, multicast to both
+//     (TMA multicast within this GPU's memory).  A 64-token stage then costs
+//     each CTA 32 KB of L2 reads instead of 48 KB; the MMAs are unchanged
+//     (one CTA, M = 128).  A stage slot is free again once both CTAs' MMAs
+//     have read it: each MMA thread releases it in both CTAs with one
+//     multicast commit.
+//   * Jobs: whole tile pairs with the full token range first, in waves of
+//     one pair per cluster (every cluster of a wave sweeps the tokens at the
+//     same pace, so each X slab is read from HBM about once per wave and
+//     re-served from L2); the pairs left over after the last full wave are
+//     split along the tokens into `ks` pieces to balance the final wave.
 //   * Results are added to S with fp32 atomics: element (r, c), r <= c, goes
 //     to S[r][c] and, for r < c, also to S[c][r].
 #include <algorithm>
@@ -61,40 +69,44 @@ struct SyrkSchedule {
   int kb_total;  // token slabs of BK
   int n_i;       // row blocks of BM
   int tiles;     // tiles touching the upper triangle
-  int full;      // jobs covering a whole tile (multiple of the grid)
-  int rem;       // tiles split into pieces
-  int ks;        // pieces per split tile
+  int pairs;     // tile pairs (row blocks 2m, 2m + 1 of one column block)
+  int full;      // jobs covering a whole pair (multiple of the clusters)
+  int rem;       // pairs split into pieces
+  int ks;        // pieces per split pair
   int jobs;
 };
 
-__device__ __forceinline__ void tile_of(int t, int n_i, int& ti, int& tj) {
-  // Column block tj of 256 holds the row blocks ti < min(n_i, 2 tj + 2).
+// Column block tj of 256 holds the row blocks ti < min(n_i, 2 tj + 2):
+// ceil(that / 2) pairs.  Pair p -> (first row block ti0 = 2m, tj).  With an
+// odd count the pair's second tile lies past d (row block n_i) and adds
+// nothing.
+__device__ __forceinline__ void pair_of(int p, int n_i, int& ti0, int& tj) {
   int j = 0;
   for (;;) {
-    const int c = min(n_i, 2 * j + 2);
-    if (t < c) break;
-    t -= c;
+    const int c = (min(n_i, 2 * j + 2) + 1) / 2;
+    if (p < c) break;
+    p -= c;
     ++j;
   }
-  ti = t;
+  ti0 = 2 * p;
   tj = j;
 }
 
-__device__ __forceinline__ void job_of(const SyrkSchedule& s, int job, int& ti, int& tj, int& k0,
+__device__ __forceinline__ void job_of(const SyrkSchedule& s, int job, int& ti0, int& tj, int& k0,
                                        int& k1) {
-  int tile;
+  int pair;
   if (job < s.full) {
-    tile = job;
+    pair = job;
     k0 = 0;
     k1 = s.kb_total;
   } else {
     const int jj = job - s.full;
     const int piece = jj / s.rem;
-    tile = s.full + jj % s.rem;
+    pair = s.full + jj % s.rem;
     k0 = static_cast<int>(static_cast<long long>(piece) * s.kb_total / s.ks);
     k1 = static_cast<int>(static_cast<long long>(piece + 1) * s.kb_total / s.ks);
   }
-  tile_of(tile, s.n_i, ti, tj);
+  pair_of(pair, s.n_i, ti0, tj);
 }
 
 // Token-major boxes: 64 channels (128 bytes) x BK tokens = 8 KB each.
@@ -123,10 +135,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  const int rank = static_cast<int>(cluster_ctarank());   // 0 or 1 within the pair
+  const int cid = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), 1);
+      mbar_init(empty_bar(i), 2);   // released by both CTAs' MMAs
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
@@ -142,7 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before either multicasts into the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -152,32 +167,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int job = blockIdx.x; ok && job < s.jobs; job += gridDim.x) {
-        int ti, tj, k0, k1;
-        job_of(s, job, ti, tj, k0, k1);
+      for (int job = cid; ok && job < s.jobs; job += nclusters) {
+        int ti0, tj, k0, k1;
+        job_of(s, job, ti0, tj, k0, k1);
+        const int ti = ti0 + rank;
         for (int kb = k0; kb < k1; ++kb) {
+          // the slot is free once both CTAs' MMAs have read it
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault)) {
             ok = false;
             break;
           }
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          // own A, own half of B to both CTAs; the other half comes from the peer
           mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
           if constexpr (TOKMAJOR) {
 #pragma unroll
             for (int c = 0; c < BM / TM_BOX; ++c)
               tma_load_2d(sa + c * TM_BOX_BYTES, &tm_a, full_bar(stage), ti * BM + c * TM_BOX, kb * BK);
 #pragma unroll
-            for (int c = 0; c < BN / TM_BOX; ++c)
-              tma_load_2d(sa + A_BYTES + c * TM_BOX_BYTES, &tm_b, full_bar(stage), tj * BN + c * TM_BOX,
-                          kb * BK);
+            for (int c = rank * (BN / TM_BOX / 2); c < (rank + 1) * (BN / TM_BOX / 2); ++c)
+              tma_load_2d_multicast(sa + A_BYTES + c * TM_BOX_BYTES, &tm_b, full_bar(stage),
+                                    tj * BN + c * TM_BOX, kb * BK, 0x3);
           } else {
             tma_load_2d(sa, &tm_a, full_bar(stage), kb * BK, ti * BM);
-            tma_load_2d(sa + A_BYTES, &tm_b, full_bar(stage), kb * BK, tj * BN);
+            tma_load_2d_multicast(sa + A_BYTES + rank * (B_BYTES / 2), &tm_b, full_bar(stage), kb * BK,
+                                  tj * BN + rank * (BN / 2), 0x3);
           }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
+        }
+      }
+      // Before this CTA may exit, every release the peer sends to its slots
+      // must have landed: wait for one more turn of the ring.
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
@@ -191,9 +219,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int job = blockIdx.x; ok && job < s.jobs; job += gridDim.x) {
-        int ti, tj, k0, k1;
-        job_of(s, job, ti, tj, k0, k1);
+      for (int job = cid; ok && job < s.jobs; job += nclusters) {
+        int ti0, tj, k0, k1;
+        job_of(s, job, ti0, tj, k0, k1);
         for (int c0 = k0; ok && c0 < k1; c0 += CH) {
           const int c1 = min(k1, c0 + CH);
           if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, fault)) {
@@ -226,7 +254,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   static_cast<uint64_t>(TOKMAJOR ? (k * UK * 128) >> 4 : (k * UK * 2) >> 4);
               tc_mma_f16(d_tmem, da + off, db + off, idesc, (kb > c0 || k > 0) ? 1u : 0u);
             }
-            tc_commit(empty_bar(stage));  // frees the slot when these MMAs finish
+            tc_commit_multicast(empty_bar(stage), 0x3);  // frees the slot (in both CTAs) when these MMAs finish
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -253,9 +281,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     const int d = s.d;
     bool ok = true;
-    for (int job = blockIdx.x; ok && job < s.jobs; job += gridDim.x) {
-      int ti, tj, k0, k1;
-      job_of(s, job, ti, tj, k0, k1);
+    for (int job = cid; ok && job < s.jobs; job += nclusters) {
+      int ti0, tj, k0, k1;
+      job_of(s, job, ti0, tj, k0, k1);
+      const int ti = ti0 + rank;
       float sum[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sum[i] = 0.f;
@@ -308,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();   // neither CTA leaves while the other may still use its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -348,6 +377,7 @@ bool make_x_map(CUtensorMap* m, const void* X, int64_t d, int64_t n_tok, int64_t
 }  // namespace
 
 // Host-side schedule (also used by the tests through gptq_internal_*).
+// grid_max: clusters (pairs of CTAs) available.
 static SyrkSchedule make_schedule(int64_t d, int64_t n_tok, int grid_max) {
   SyrkSchedule s{};
   s.d = static_cast<int>(d);
@@ -355,10 +385,15 @@ static SyrkSchedule make_schedule(int64_t d, int64_t n_tok, int grid_max) {
   s.n_i = static_cast<int>((d + BM - 1) / BM);
   const int n_j = static_cast<int>((d + BN - 1) / BN);
   s.tiles = 0;
-  for (int j = 0; j < n_j; ++j) s.tiles += (s.n_i < 2 * j + 2) ? s.n_i : 2 * j + 2;
+  s.pairs = 0;
+  for (int j = 0; j < n_j; ++j) {
+    const int c = (s.n_i < 2 * j + 2) ? s.n_i : 2 * j + 2;
+    s.tiles += c;
+    s.pairs += (c + 1) / 2;
+  }
   const int G = grid_max;
-  s.full = (s.tiles / G) * G;
-  s.rem = s.tiles - s.full;
+  s.full = (s.pairs / G) * G;
+  s.rem = s.pairs - s.full;
   s.ks = 1;
   if (s.rem > 0) {
     // Pieces of at least 8 slabs; pick the split that best fills the last
@@ -382,12 +417,12 @@ gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64
                                   float* S, cudaStream_t st) {
   CUtensorMap tm_a, tm_b;
   if (!make_x_map(&tm_a, X, d, n_tok, ldx, BM, tok_major) ||
-      !make_x_map(&tm_b, X, d, n_tok, ldx, BN, tok_major))
+      !make_x_map(&tm_b, X, d, n_tok, ldx, BN / 2, tok_major))
     return GPTQ_ERR_CUDA;
   int* fault = fault_word_ptr();
   if (!fault) return GPTQ_ERR_CUDA;
-  const int sms = sm_count();
-  SyrkSchedule s = make_schedule(d, n_tok, sms);
+  const int clusters = sm_count() / 2;
+  SyrkSchedule s = make_schedule(d, n_tok, clusters);
   auto kern = tok_major ? hessian_syrk_kernel<true> : hessian_syrk_kernel<false>;
   static int attr_dev[2] = {-1, -1};   // the attribute is set once per device and layout
   int dev = 0;
@@ -396,8 +431,20 @@ gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64
     GPTQ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     attr_dev[tok_major ? 1 : 0] = dev;
   }
-  const int grid = std::min(sms, s.jobs);
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, s, S, fault);
+  // one cluster of two CTAs per pair job in flight
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * std::min(clusters, s.jobs));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  GPTQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, tm_a, tm_b, s, S, fault));
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
@@ -408,7 +455,7 @@ gptq_status_t launch_hessian_syrk(const void* X, int64_t d, int64_t n_tok, int64
 // tiles, pieces, jobs) for a given problem and grid.
 extern "C" GPTQ_API void gptq_internal_syrk_schedule(int64_t d, int64_t n_tok, int grid, int32_t* out5) {
   gptq::SyrkSchedule s = gptq::make_schedule(d, n_tok, grid);
-  out5[0] = s.tiles;
+  out5[0] = s.pairs;
   out5[1] = s.full;
   out5[2] = s.rem;
   out5[3] = s.ks;

@@ -145,24 +145,28 @@ def test_pack_rejects_bad_args(lib):
 def schedule(lib, d, n_tok, grid):
     out = (ctypes.c_int32 * 5)()
     lib.gptq_internal_syrk_schedule(ctypes.c_int64(d), ctypes.c_int64(n_tok), grid, out)
-    return dict(zip(("tiles", "full", "rem", "ks", "jobs"), list(out)))
+    return dict(zip(("pairs", "full", "rem", "ks", "jobs"), list(out)))
 
 
-def upper_tiles(d):
-    """Tiles of 128 rows x 256 cols that hold some (r, c) with r <= c."""
-    n = 0
-    for ti in range((d + 127) // 128):
-        for tj in range((d + 255) // 256):
-            if 128 * ti <= 256 * tj + 255:
-                n += 1
-    return n
+def upper_tile_pairs(d):
+    """Tiles of 128 rows x 256 cols that hold some (r, c) with r <= c, counted
+    per column block; each column block's tiles are taken two row blocks at a
+    time (the two CTAs of a cluster), so a block with c tiles has ceil(c/2)
+    pairs.  Returns (tiles, pairs)."""
+    tiles = pairs = 0
+    for tj in range((d + 255) // 256):
+        c = sum(1 for ti in range((d + 127) // 128) if 128 * ti <= 256 * tj + 255)
+        tiles += c
+        pairs += (c + 1) // 2
+    return tiles, pairs
 
 
 @pytest.mark.parametrize("d", [32, 256, 512, 544, 4096, 5120, 11008, 13824])
 def test_syrk_schedule_covers_all_tiles(lib, d):
-    s = schedule(lib, d, 262144, 148)
-    assert s["tiles"] == upper_tiles(d)
-    assert s["full"] % 148 == 0 and s["full"] + s["rem"] == s["tiles"]
+    s = schedule(lib, d, 262144, 74)
+    tiles, pairs = upper_tile_pairs(d)
+    assert s["pairs"] == pairs and tiles <= 2 * pairs
+    assert s["full"] % 74 == 0 and s["full"] + s["rem"] == s["pairs"]
     assert s["jobs"] == s["full"] + s["rem"] * s["ks"]
     assert s["ks"] >= 1 and (s["rem"] > 0 or s["ks"] == 1)
     # each piece keeps at least 8 slabs of 64 tokens
@@ -170,7 +174,7 @@ def test_syrk_schedule_covers_all_tiles(lib, d):
 
 
 def test_syrk_schedule_small_token_count(lib):
-    s = schedule(lib, 512, 2048, 148)
+    s = schedule(lib, 512, 2048, 74)
     assert s["ks"] <= 2048 // 64 // 8
 
 
