@@ -31,6 +31,9 @@
 // Cost ~ 2 d^3 / 3 flop, all of it in the tensor-core GEMMs except O(d nb^2).
 #include <algorithm>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 #include "tgemm.cuh"
 
@@ -167,6 +170,7 @@ struct PanelArgs {
   int* status;
   const float* zlo;  // [n] low parts of the diagonal of Z
   int split;         // CTAs per role tile (1, 2 or 4)
+  float* Mg;         // [NB][NB] (L_kk^-1)^T, from the factor kernel to the role kernel
 };
 
 __device__ __forceinline__ void store_split(float* hi, float* lo, int64_t off, float v) {
@@ -193,8 +197,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 }
 
 // Factor the b x b lower block D = Z[k..k+b)^2 (b a multiple of 32, at most
-// NB) and write Mt = (L^-1)^T (Mt[c][i] = L^-1[i][c], zero above the
-// diagonal of L^-1 and outside b) to shared memory.
+// NB) and write Mt = (L^-1)^T (Mt[c][i] = L^-1[i][c]) to shared memory,
+// which the caller has zeroed (so that Mt is zero above the diagonal of
+// L^-1 and outside b).
 //
 // Blocked over 32-wide sub-panels s, so that the column-by-column chain of
 // the factorization runs inside one warp and block barriers are needed only
@@ -233,7 +238,6 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
       else v.w += lo;
     }
     *reinterpret_cast<float4*>(Ls + i * LDM + c4) = v;
-    *reinterpret_cast<float4*>(Mt + i * LDM + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   bool bad = false;
@@ -522,68 +526,72 @@ __device__ __forceinline__ void role_products(const PanelArgs& p, bool xrole, in
   }
 }
 
-// One step k of the factorization.  CTA 0 writes the diagonal block of U and
-// of B; the other CTAs each take `split` consecutive parts (128/split rows)
-// of one role tile: the Acc tiles left of the diagonal block (X role), then
-// the panel tiles below it (P role).  Every CTA factors the diagonal block
-// itself, while its role operand is fetched.
-__global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
+// One step k of the factorization, in two kernels.
+//   panel_factor_kernel (one CTA): factor the diagonal block and write
+//     M^T = (L_kk^-1)^T to Mg.
+//   panel_role_kernel: each CTA but the last takes `split` consecutive parts
+//     (128/split rows) of one role tile: the Acc tiles left of the diagonal
+//     block (X role), then the panel tiles below it (P role).  The last CTA
+//     writes M itself: the diagonal block of U and B rows k..k+b.
+// The factorization is the step's sequential chain, so it runs alone on one
+// SM and writes only what the next kernel needs; the rest of the GPU stays
+// free for the update GEMM of the previous step.
+__global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
   extern __shared__ __align__(16) float sm[];
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
-  float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
-  float* Ls = T + NB * LDM;          // [NB][LDM]  diagonal block, then L_kk
+  float* Ls = Mt + NB * LDM;         // [NB][LDM]  diagonal block, then L_kk
   float* rdiag = Ls + NB * LDM;      // [NB]       1 / diag(L_kk)
   float* Tm = rdiag + NB;            // [3][32][TMLD] level products
   float* LT = Tm;                    // [32][LDM] transposed sub-panel (shares Tm's space)
   float* colbuf = LT + 32 * LDM;     // [2][32]
   float* LssT = colbuf + 64;         // [32][LST] transposed diagonal sub-block
+  const int t = threadIdx.x;
+  for (int q = t; q < NB * (NB / 4); q += PT)
+    *reinterpret_cast<float4*>(Mt + (q / (NB / 4)) * LDM + (q % (NB / 4)) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  // Launched with programmatic dependent launch: Z comes from the previous
+  // kernels.  The role kernel that follows is let in only at the end: its
+  // CTAs would otherwise sit on SMs, waiting, for the whole factorization,
+  // and keep them from the update GEMM that runs beside it.
+  griddep_wait();
+  const bool notpd = factor_invert_blocked(p.Z, p.zlo, p.n, p.k, p.b, Mt, Ls, rdiag, Tm, LT, colbuf, LssT);
+  if (t == 0 && notpd) atomicOr(p.status, kStatNotPD);
+  __syncthreads();
+  for (int idx = t; idx < NB * (NB / 4); idx += PT) {
+    const int c = idx / (NB / 4), r4 = (idx % (NB / 4)) * 4;
+    *reinterpret_cast<float4*>(p.Mg + c * NB + r4) = *reinterpret_cast<const float4*>(Mt + c * LDM + r4);
+  }
+  griddep_launch_dependents();
+}
+
+__global__ void __launch_bounds__(PT, 1) panel_role_kernel(PanelArgs p) {
+  extern __shared__ __align__(16) float sm[];
+  float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
+  float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
   const int n = p.n, k = p.k, b = p.b;
   const int64_t ldz = n;
   const int t = threadIdx.x;
-  const int role = blockIdx.x;
-  const int tile = role >= 1 ? (role - 1) / p.split : 0;
-  const int part = role >= 1 ? (role - 1) % p.split : 0;
-  const bool xrole = role >= 1 && tile < p.n_acc;
+  const bool diag_cta = blockIdx.x == gridDim.x - 1;
+  const int tile = blockIdx.x / p.split;
+  const int part = blockIdx.x % p.split;
+  const bool xrole = tile < p.n_acc;
   const int ptile = tile - p.n_acc;  // P role: panel tile index
   const int prow = NB / p.split;     // rows of the P operand this CTA needs
-  // Launched with programmatic dependent launch: Z and B come from the
-  // previous kernels.
+  // Z, B and M come from the previous kernels.
   griddep_wait();
   griddep_launch_dependents();
-
-  // Role operand tile, fetched while the diagonal block is factored.
-  if (role >= 1) {
-    if (xrole) {  // T[q][cc] = Acc[k + q][cbase + cc], all 128 q
-      const int cbase = tile * NB;
-      for (int q = t; q < NB * (NB / 4); q += PT) {
-        const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
-        const bool ok = rr < b && cbase + c4 < k;
-        const float* src = p.Z + static_cast<int64_t>(k + rr) * ldz + cbase + c4;
-        cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
-      }
-    } else {      // T[rr][q] = A[rbase + rr][k + q], this CTA's rows only
-      const int rbase = k + b + ptile * NB + part * prow;
-      for (int q = t; q < prow * (NB / 4); q += PT) {
-        const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
-        const bool ok = rbase + rr < n && c4 < b;
-        const float* src = p.Z + static_cast<int64_t>(rbase + rr) * ldz + k + c4;
-        cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
-      }
-    }
+  for (int q = t; q < NB * (NB / 4); q += PT) {
+    const int c = q / (NB / 4), r4 = (q % (NB / 4)) * 4;
+    cp_async16(Mt + c * LDM + r4, p.Mg + c * NB + r4, true);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
-
-  const bool notpd = factor_invert_blocked(p.Z, p.zlo, ldz, k, b, Mt, Ls, rdiag, Tm, LT, colbuf, LssT);
-  if (role == 0 && t == 0 && notpd) atomicOr(p.status, kStatNotPD);
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
-
-  if (role == 0) {
+  if (diag_cta) {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
     // X[k + r][k + c] = M[r][c] = Mt[c][r] for c <= r: U[n-1-k-r][n-1-k-c],
     // and B rows k..k+b (B[k + c][r] = Mt[c][r]).
-    for (int idx = t; idx < b * b; idx += PT) {
-      const int r = idx / b, c = idx % b;
-      if (c <= r) p.U[static_cast<int64_t>(n - 1 - k - r) * n + (n - 1 - k - c)] = Mt[c * LDM + r];
+    for (int idx = t; idx < NB * NB; idx += PT) {
+      const int r = idx / NB, c = idx % NB;
+      if (r < b && c <= r) p.U[static_cast<int64_t>(n - 1 - k - r) * n + (n - 1 - k - c)] = Mt[c * LDM + r];
     }
     for (int idx = t; idx < b * (NB / 4); idx += PT) {
       const int c = idx / (NB / 4), r4 = (idx % (NB / 4)) * 4;
@@ -592,6 +600,26 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
     }
     return;
   }
+  if (xrole) {  // T[q][cc] = Acc[k + q][cbase + cc], all 128 q
+    const int cbase = tile * NB;
+    for (int q = t; q < NB * (NB / 4); q += PT) {
+      const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
+      const bool ok = rr < b && cbase + c4 < k;
+      const float* src = p.Z + static_cast<int64_t>(k + rr) * ldz + cbase + c4;
+      cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
+    }
+  } else {      // T[rr][q] = A[rbase + rr][k + q], this CTA's rows only
+    const int rbase = k + b + ptile * NB + part * prow;
+    for (int q = t; q < prow * (NB / 4); q += PT) {
+      const int rr = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
+      const bool ok = rbase + rr < n && c4 < b;
+      const float* src = p.Z + static_cast<int64_t>(rbase + rr) * ldz + k + c4;
+      cp_async16(T + rr * LDM + c4, ok ? src : p.Z, ok);
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   if (p.split == 4)
     role_products<1>(p, xrole, xrole ? tile : ptile, part, Mt, T);
   else if (p.split == 2)
@@ -604,7 +632,7 @@ __global__ void __launch_bounds__(PT, 1) panel_step_kernel(PanelArgs p) {
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct PrepLayout {
-  size_t status, lam, keys, zlo, Z, Bhi, Blo, total;
+  size_t status, lam, keys, zlo, Z, Mg, Bhi[2], Blo[2], total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -622,19 +650,65 @@ static PrepLayout prep_layout(int64_t d) {
   off = align256(off + sizeof(float) * d);
   L.Z = off;
   off = align256(off + sizeof(float) * d * d);
-  L.Bhi = off;
-  off = align256(off + sizeof(float) * d * NB);
-  L.Blo = off;
-  off = align256(off + sizeof(float) * d * NB);
+  L.Mg = off;
+  off = align256(off + sizeof(float) * NB * NB);
+  for (int i = 0; i < 2; ++i) {  // panel operands of even and odd steps
+    L.Bhi[i] = off;
+    off = align256(off + sizeof(float) * d * NB);
+    L.Blo[i] = off;
+    off = align256(off + sizeof(float) * d * NB);
+  }
   L.total = off;
   return L;
 }
 
 size_t prep_workspace_bytes(int64_t d) { return prep_layout(d).total; }
 
+namespace {
+
+// A second stream with two events, on which one step's update GEMM runs
+// beside the next step's factorization.  Kept in a per-device pool: a call
+// takes one for the time it enqueues its work and puts it back, so calls
+// from several host threads never share one at the same time (a later call
+// that gets the same stream only queues behind the earlier call's work).
+struct Helper {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t ev_pri = nullptr;   // recorded on the caller's stream: step ready for its rest GEMM
+  cudaEvent_t ev_rest = nullptr;  // recorded on the helper stream: rest GEMM done
+};
+
+std::mutex g_helper_mu;
+std::vector<Helper> g_helpers[64];
+
+bool take_helper(int dev, Helper& h) {
+  {
+    std::lock_guard<std::mutex> lock(g_helper_mu);
+    if (!g_helpers[dev].empty()) {
+      h = g_helpers[dev].back();
+      g_helpers[dev].pop_back();
+      return true;
+    }
+  }
+  if (cudaStreamCreateWithFlags(&h.stream, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&h.ev_pri, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h.ev_rest, cudaEventDisableTiming) != cudaSuccess) {
+    if (h.ev_pri) cudaEventDestroy(h.ev_pri);
+    cudaStreamDestroy(h.stream);
+    return false;
+  }
+  return true;
+}
+
+void give_helper(int dev, const Helper& h) {
+  std::lock_guard<std::mutex> lock(g_helper_mu);
+  g_helpers[dev].push_back(h);
+}
+
+}  // namespace
+
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, int64_t n_seen,
                              float damp, bool desc_act, float* U, int32_t* perm, void* ws,
-                             cudaStream_t st) {
+                             bool overlap, cudaStream_t st) {
   const int d = static_cast<int>(d64);
   const PrepLayout L = prep_layout(d64);
   char* base = static_cast<char*>(ws);
@@ -643,8 +717,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   auto* keys = reinterpret_cast<unsigned long long*>(base + L.keys);
   float* Z = reinterpret_cast<float*>(base + L.Z);
   float* zlo = reinterpret_cast<float*>(base + L.zlo);
-  float* Bhi = reinterpret_cast<float*>(base + L.Bhi);
-  float* Blo = reinterpret_cast<float*>(base + L.Blo);
+  float* Mg = reinterpret_cast<float*>(base + L.Mg);
   const double hscale = 2.0 / static_cast<double>(n_seen);
 
   GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
@@ -663,12 +736,35 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     prep_diag_kernel<<<(d + 255) / 256, 256, 0, st>>>(S, diag, perm, d, hscale, lam, Z, zlo, status);
     GPTQ_LAUNCH_CHECK();
   }
-  const size_t smem = sizeof(float) * (3 * NB * LDM + NB + 32 * LDM + 64 + 32 * LST);
-  GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)));
+  const size_t smem_factor = sizeof(float) * (2 * NB * LDM + NB + 32 * LDM + 64 + 32 * LST);
+  const size_t smem_role = sizeof(float) * (2 * NB * LDM);
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem_factor)));
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_role_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem_role)));
   const int sms = sm_count();
-  for (int k = 0; k < d; k += NB) {
+
+  // Step k: factor the diagonal block (one CTA), the role products, then the
+  // update of the trailing rows by B_k, split into two launches.  The
+  // "priority" tiles (the next step's diagonal row block and column block)
+  // are all that step k + 1's factorization and role products read, so with
+  // `overlap` only they run before step k + 1 on the caller's stream, and the
+  // "rest" runs on a helper stream beside step k + 1's factor and role
+  // kernels.  Step k + 1's own update touches the rest's tiles, so it waits
+  // for them; its panel operands go to the other of two B buffers, since the
+  // rest of step k still reads the first.  Without `overlap` the same
+  // launches run in the same order on one stream.
+  Helper h;
+  int dev = 0;
+  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+  if (overlap && (dev < 0 || dev >= 64 || !take_helper(dev, h))) overlap = false;
+  gptq_status_t result = GPTQ_OK;
+  bool rest_pending = false;  // a rest GEMM is queued on the helper stream
+  for (int k = 0; k < d && result == GPTQ_OK; k += NB) {
     const int b = std::min(NB, d - k);
+    const int par = (k / NB) & 1;
+    float* Bhi = reinterpret_cast<float*>(base + L.Bhi[par]);
+    float* Blo = reinterpret_cast<float*>(base + L.Blo[par]);
     PanelArgs pa;
     pa.Z = Z;
     pa.n = d;
@@ -680,33 +776,73 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     pa.U = U;
     pa.status = status;
     pa.zlo = zlo;
+    pa.Mg = Mg;
     const int n_pan = (d - k - b + NB - 1) / NB;
-    // Split the role tiles over more CTAs while one wave of CTAs still holds
-    // them all (every CTA also factors the diagonal block).
     const int tiles = pa.n_acc + n_pan;
-    pa.split = (1 + 4 * tiles <= sms) ? 4 : (1 + 2 * tiles <= sms) ? 2 : 1;
-    GPTQ_CUDA_TRY(launch_pdl(panel_step_kernel, dim3(1 + tiles * pa.split), dim3(PT), smem, st, pa));
-    GPTQ_LAUNCH_CHECK();
-    if (k + b < d) {
-      TGemmArgs g;
-      g.M = d - k - b;
-      g.N = d;
-      g.K = NB;
-      g.alpha = -1.f;
-      g.beta = 1.f;
-      g.C = Z + static_cast<int64_t>(k + b) * d;
-      g.ldc = d;
-      g.lower = 1;
-      g.row_off = k + b;
-      g.col_off = 0;
-      g.diag_lo = zlo;
-      const gptq_status_t s = launch_tgemm_3xtf32(Bhi + static_cast<int64_t>(k + b) * NB,
-                                                  Blo + static_cast<int64_t>(k + b) * NB, NB, Bhi, Blo,
-                                                  NB, g, status, st);
-      if (s != GPTQ_OK) return s;
+    pa.split = (4 * tiles < sms) ? 4 : (2 * tiles < sms) ? 2 : 1;
+    if (cudaSuccess != launch_pdl(panel_factor_kernel, dim3(1), dim3(PT), smem_factor, st, pa) ||
+        cudaSuccess != cudaGetLastError()) {
+      result = GPTQ_ERR_CUDA;
+      break;
     }
+    if (cudaSuccess != launch_pdl(panel_role_kernel, dim3(tiles * pa.split + 1), dim3(PT), smem_role, st,
+                                  pa) ||
+        cudaSuccess != cudaGetLastError()) {
+      result = GPTQ_ERR_CUDA;
+      break;
+    }
+    if (k + b >= d) break;
+    TGemmArgs g;
+    g.M = d - k - b;
+    g.N = d;
+    g.K = NB;
+    g.alpha = -1.f;
+    g.beta = 1.f;
+    g.C = Z + static_cast<int64_t>(k + b) * d;
+    g.ldc = d;
+    g.lower = 1;
+    g.row_off = k + b;
+    g.col_off = 0;
+    g.diag_lo = zlo;
+    g.pri_nt = (k + b) / NB;
+    const float* Ahi = Bhi + static_cast<int64_t>(k + b) * NB;
+    const float* Alo = Blo + static_cast<int64_t>(k + b) * NB;
+    // The priority tiles overwrite tiles that the previous rest GEMM updates.
+    if (rest_pending && cudaSuccess != cudaStreamWaitEvent(st, h.ev_rest, 0)) {
+      result = GPTQ_ERR_CUDA;
+      break;
+    }
+    g.subset = 1;
+    result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, st);
+    if (result != GPTQ_OK) break;
+    g.subset = 2;
+    if (tgemm_tile_count(g) == 0) continue;
+    if (!overlap) {
+      result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, st);
+      continue;
+    }
+    // Leave an SM for the next step's factorization.
+    g.max_ctas = sms - 1;
+    if (cudaSuccess != cudaEventRecord(h.ev_pri, st) ||
+        cudaSuccess != cudaStreamWaitEvent(h.stream, h.ev_pri, 0)) {
+      result = GPTQ_ERR_CUDA;
+      break;
+    }
+    result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, h.stream);
+    if (result != GPTQ_OK) break;
+    if (cudaSuccess != cudaEventRecord(h.ev_rest, h.stream)) {
+      result = GPTQ_ERR_CUDA;
+      break;
+    }
+    rest_pending = true;
   }
-  return GPTQ_OK;
+  if (overlap) {
+    // Join: the caller's stream ends after the helper stream's last work.
+    if (rest_pending && cudaSuccess != cudaStreamWaitEvent(st, h.ev_rest, 0) && result == GPTQ_OK)
+      result = GPTQ_ERR_CUDA;
+    give_helper(dev, h);
+  }
+  return result;
 }
 
 }  // namespace gptq

@@ -15,6 +15,9 @@ namespace gptq {
 
 size_t prep_workspace_bytes(int64_t d);
 gptq_status_t read_workspace_status(const void* ws, cudaStream_t st);
+gptq_status_t prepare_hinv_call(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
+                                const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
+                                size_t ws_bytes, bool overlap, gptq_stream_t stream);
 
 namespace {
 
@@ -22,10 +25,12 @@ constexpr int64_t kMaxDCol = GPTQ_NOALLOC_MAX_D_COL;
 constexpr size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Room for the prepare workspace at d_col = kMaxDCol: status and damping
 // words, the 64-bit sort keys, the low parts of the work matrix's diagonal,
-// the d x d work matrix and the two d x 128 panel operands.  Each call
-// checks it against prep_workspace_bytes().
+// the d x d work matrix, the 128 x 128 inverse of a diagonal block, and two
+// pairs of d x 128 panel operands.  Each call checks it against
+// prep_workspace_bytes().
 constexpr size_t kScratchBytes = 256 + 256 + round256(8 * kMaxDCol) + round256(4 * kMaxDCol) +
-                                 round256(4 * kMaxDCol * kMaxDCol) + 2 * round256(4 * kMaxDCol * 128);
+                                 round256(4 * kMaxDCol * kMaxDCol) + round256(4 * 128 * 128) +
+                                 4 * round256(4 * kMaxDCol * 128);
 
 static __device__ __align__(256) unsigned char g_prep_scratch[kScratchBytes];
 
@@ -57,8 +62,10 @@ extern "C" GPTQ_API gptq_status_t gptq_prepare_hinv_noalloc(const float* S, cons
   if (d_col > 0 && gptq::prep_workspace_bytes(d_col) > gptq::kScratchBytes) return GPTQ_ERR_WORKSPACE;
   void* ws = gptq::scratch_address();
   if (!ws) return GPTQ_ERR_CUDA;
-  const gptq_status_t s =
-      gptq_prepare_hinv(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream);
+  // Every launch on the caller's stream: no second stream or events are
+  // created for this call.
+  const gptq_status_t s = gptq::prepare_hinv_call(S, diag, d_col, n_seen, cfg, U, perm, ws,
+                                                  gptq::kScratchBytes, false, stream);
   if (s != GPTQ_OK) return s;
   // The status word of the call sits in the library's array, where the
   // caller cannot read it: wait for the call and report it here.

@@ -33,22 +33,38 @@ struct TGemmSched {
   int m_tiles, n_tiles, k_blocks, tiles;
 };
 
-__device__ __forceinline__ int n_tiles_for_row(const TGemmArgs& a, const TGemmSched& s, int mt) {
-  if (!a.lower) return s.n_tiles;
+// Tiles of tile row mt below or on the diagonal (all of them without `lower`).
+__host__ __device__ __forceinline__ int row_tiles(const TGemmArgs& a, int n_tiles, int mt) {
+  if (!a.lower) return n_tiles;
   const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM - 1 -
                         a.col_off;
   if (lim < 0) return 0;
-  return static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
+  return static_cast<int>(lim / BN + 1 < n_tiles ? lim / BN + 1 : n_tiles);
 }
 
+// Tiles of row mt in the launch's subset.
+__host__ __device__ __forceinline__ int subset_row_tiles(const TGemmArgs& a, int n_tiles, int mt) {
+  const int c = row_tiles(a, n_tiles, mt);
+  if (a.subset == 0) return c;
+  const int has_pri = (a.pri_nt < c) ? 1 : 0;
+  if (a.subset == 1) return mt == 0 ? c : has_pri;
+  return mt == 0 ? 0 : c - has_pri;
+}
+
+// The t-th tile of the subset, rows in order, columns in order within a row.
 __device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
                                             int& nt) {
   for (mt = 0; mt < s.m_tiles; ++mt) {
-    const int c = n_tiles_for_row(a, s, mt);
+    const int c = subset_row_tiles(a, s.n_tiles, mt);
     if (t < c) break;
     t -= c;
   }
-  nt = t;
+  if (a.subset == 1 && mt > 0)
+    nt = a.pri_nt;
+  else if (a.subset == 2 && t >= a.pri_nt)
+    nt = t + 1;
+  else
+    nt = t;
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -293,15 +309,7 @@ TGemmSched make_sched(const TGemmArgs& a) {
   s.n_tiles = (a.N + BN - 1) / BN;
   s.k_blocks = (a.K + BK - 1) / BK;
   s.tiles = 0;
-  for (int mt = 0; mt < s.m_tiles; ++mt) {
-    int c = s.n_tiles;
-    if (a.lower) {
-      const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM -
-                            1 - a.col_off;
-      c = lim < 0 ? 0 : static_cast<int>(std::min<long long>(s.n_tiles, lim / BN + 1));
-    }
-    s.tiles += c;
-  }
+  for (int mt = 0; mt < s.m_tiles; ++mt) s.tiles += subset_row_tiles(a, s.n_tiles, mt);
   return s;
 }
 
@@ -328,7 +336,8 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
                                        SMEM_BYTES));
     attr_dev = dev;
   }
-  const int grid = std::min(sm_count(), s.tiles);
+  int grid = std::min(sm_count(), s.tiles);
+  if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
   GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, m_ahi, m_alo,
                            m_bhi, m_blo, args, s, fault));
   GPTQ_LAUNCH_CHECK();

@@ -31,6 +31,13 @@ struct TGemmArgs {
   // update (Knuth two-sum) is added to diag_lo[col_off + n], so that
   // C + diag_lo carries the running diagonal to about twice fp32 precision.
   float* diag_lo = nullptr;
+  // Optional tile subsets, for splitting one update into two launches:
+  // subset 1 takes the tiles of the first tile row (mt == 0) and of tile
+  // column pri_nt; subset 2 takes all the others; 0 takes every tile.
+  int subset = 0;
+  int pri_nt = 0;
+  // At most this many CTAs (0: one per SM).
+  int max_ctas = 0;
 };
 
 // hi: x rounded to a TF32 value (10 explicit mantissa bits, ties away);
@@ -53,7 +60,8 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
                                   const float* B_hi, const float* B_lo, int64_t ldb,
                                   const TGemmArgs& args, int* fault, cudaStream_t st);
 
-// Number of 128 x 128 output tiles the launch above would process.
+// Number of 128 x 128 output tiles the launch above would process (of its
+// subset).
 int tgemm_tile_count(const TGemmArgs& args);
 
 }  // namespace gptq
