@@ -20,8 +20,8 @@
 //   * the running right-hand side Acc = I - L[:, <k] X[<k, :] of L X = I in
 //     the lower-left part, where the already-used panels of L used to be.
 // Step k:
-//   panel kernel   factor the diagonal block, M = L_kk^-1 (every CTA redoes
-//                  this small factorization), then in parallel
+//   factor kernel  factor the diagonal block, M = L_kk^-1 (one CTA);
+//   role kernel    in parallel
 //                    X_k = [M Acc_k[:, <k], M]   -> U rows (reversed), B rows
 //                    P   = A[>k, k] M^T          -> B rows; the panel is zeroed
 //                  where B = [X_k^T ; P] (hi/lo TF32 split) is n x 128;
@@ -205,18 +205,86 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 // the factorization runs inside one warp and block barriers are needed only
 // between the sub-panel phases:
 //   F  one warp factors the 32 x 32 diagonal sub-block in registers (lane i
-//      holds row i; each column's entries are broadcast by shuffles);
+//      holds row i; each column's entries are broadcast through shared
+//      memory);
 //   T  the rows below, one thread per row, solve x L_ss^T = d by forward
 //      substitution (L_ts = D_ts L_ss^-T);
 //   U  the trailing sub-blocks of the diagonal block get D_tu -= L_ts L_us^T.
-// Then L^-1 is built by blocks: the inverse of each diagonal sub-block by
-// one warp (back substitution per row, no cross-lane traffic), and the
-// sub-blocks below the diagonal level by level,
-//   M_ts = -M_tt sum_{u=s}^{t-1} L_tu M_us.
+// L^-1 = M is built by block rows as soon as each row of L is known: in T,
+// one more warp inverts the diagonal sub-block (M_ss, back substitution per
+// row, no cross-lane traffic); in U, the warps the update leaves idle form
+// the sums R_u = sum_{v=u}^{s-1} L_sv M_vu for u < s; in the next F, the
+// warps beside the factoring one finish M_su = -M_ss R_u.  So the inverse
+// costs one phase after the last sub-panel instead of phases of its own.
 // Returns true (in thread 0) if a pivot was not positive.
 constexpr int TMLD = 36;  // row stride of the 32 x 32 level products
 
 constexpr int LST = 36;  // row stride of the transposed 32 x 32 diagonal sub-block
+
+// Inverse of the diagonal sub-block s by one warp: lane i computes row i of
+// M_ss (back substitution), written transposed into Mt.
+__device__ __forceinline__ void invert_diag_block(int s, const float* __restrict__ Ls,
+                                                  const float* __restrict__ rdiag,
+                                                  float* __restrict__ Mt, int lane) {
+  const int w0 = 32 * s;
+  float acc[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) acc[c] = (c == lane) ? 1.f : 0.f;
+#pragma unroll
+  for (int m = 31; m >= 0; --m) {
+    const float ym = (m <= lane) ? acc[m] * rdiag[w0 + m] : 0.f;
+    Mt[(w0 + m) * LDM + w0 + lane] = ym;
+#pragma unroll
+    for (int c = 0; c < m; ++c) acc[c] = fmaf(-ym, Ls[(w0 + m) * LDM + w0 + c], acc[c]);
+  }
+}
+
+// First half of block (tb, sb) of M, sb < tb, by 128 threads (g in
+// [0, 128): row i = g % 32 of the block, columns 8 (g / 32) .. + 8):
+// R[i][c] = sum_{u=sb}^{tb-1} L_{tb,u} M_{u,sb}, into Tm slot sb.
+__device__ __forceinline__ void inverse_rows_sum(int tb, int sb, int g, const float* __restrict__ Ls,
+                                                 const float* __restrict__ Mt, float* __restrict__ Tm) {
+  const int i = g & 31, cg8 = (g >> 5) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int u = sb; u < tb; ++u) {
+    const float* li = Ls + (32 * tb + i) * LDM + 32 * u;
+#pragma unroll 2
+    for (int m = 0; m < 32; m += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(li + m);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const float4 y = *reinterpret_cast<const float4*>(Mt + (32 * sb + cg8 + cc) * LDM + 32 * u + m);
+        acc[cc] = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc[cc]))));
+      }
+    }
+  }
+  float* tm = Tm + (sb * 32 + i) * TMLD + cg8;
+  *reinterpret_cast<float4*>(tm) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  *reinterpret_cast<float4*>(tm + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+// Second half: M_{tb,sb} = -M_{tb,tb} R (same thread layout).
+__device__ __forceinline__ void inverse_rows_finish(int tb, int sb, int g, const float* __restrict__ Tm,
+                                                    float* __restrict__ Mt) {
+  const int i = g & 31, cg8 = (g >> 5) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int m = 0; m < 32; ++m) {
+    const float mv = Mt[(32 * tb + m) * LDM + 32 * tb + i];
+    const float4 y0 = *reinterpret_cast<const float4*>(Tm + (sb * 32 + m) * TMLD + cg8);
+    const float4 y1 = *reinterpret_cast<const float4*>(Tm + (sb * 32 + m) * TMLD + cg8 + 4);
+    acc[0] = fmaf(mv, y0.x, acc[0]);
+    acc[1] = fmaf(mv, y0.y, acc[1]);
+    acc[2] = fmaf(mv, y0.z, acc[2]);
+    acc[3] = fmaf(mv, y0.w, acc[3]);
+    acc[4] = fmaf(mv, y1.x, acc[4]);
+    acc[5] = fmaf(mv, y1.y, acc[5]);
+    acc[6] = fmaf(mv, y1.z, acc[6]);
+    acc[7] = fmaf(mv, y1.w, acc[7]);
+  }
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) Mt[(32 * sb + cg8 + cc) * LDM + 32 * tb + i] = -acc[cc];
+}
 
 __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* __restrict__ zlo,
                                       int64_t ldz, int k, int b,
@@ -226,23 +294,25 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
                                       float* __restrict__ LssT) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int nsub = b >> 5;
+  // The lower 4-wide chunks of the block (zero elsewhere), all copies in
+  // flight at once; then the diagonal gets its low part, hi + lo.
   for (int q = t; q < NB * (NB / 4); q += PT) {
     const int i = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < b && c4 <= i) v = *reinterpret_cast<const float4*>(Z + static_cast<int64_t>(k + i) * ldz + k + c4);
-    if (i < b && c4 <= i && i < c4 + 4) {  // the diagonal element, hi + lo
-      const float lo = zlo[k + i];
-      if (i == c4) v.x += lo;
-      else if (i == c4 + 1) v.y += lo;
-      else if (i == c4 + 2) v.z += lo;
-      else v.w += lo;
-    }
-    *reinterpret_cast<float4*>(Ls + i * LDM + c4) = v;
+    const bool ok = i < b && c4 <= i;
+    cp_async16(Ls + i * LDM + c4, ok ? Z + static_cast<int64_t>(k + i) * ldz + k + c4 : Z, ok);
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  if (t < b) Ls[t * LDM + t] += zlo[k + t];
   __syncthreads();
   bool bad = false;
   for (int s = 0; s < nsub; ++s) {
     const int c0 = 32 * s;
+    if (warp > 0 && s >= 2 && t - 32 < (s - 1) * 128) {
+      // block row s - 1 of M, second half, beside the factorization
+      inverse_rows_finish(s - 1, (t - 32) >> 7, (t - 32) & 127, Tm, Mt);
+    }
     if (warp == 0) {
       // ---- F: Cholesky of the diagonal sub-block, lane = row
       float a[32];
@@ -297,7 +367,9 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
       for (int c = 0; c < 32; ++c) LssT[c * LST + lane] = (c <= lane) ? a[c] : 0.f;
     }
     __syncthreads();
-    // ---- T: rows below the sub-block, within the diagonal block
+    // ---- T: rows below the sub-block, within the diagonal block (at most
+    //      three warps), and the inverse of the diagonal sub-block (last warp)
+    if (warp == PT / 32 - 1) invert_diag_block(s, Ls, rdiag, Mt, lane);
     if (t < b - c0 - 32) {
       float* row = Ls + (c0 + 32 + t) * LDM + c0;
       float a[32];
@@ -368,73 +440,16 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
         v.w -= acc[r][3];
         *o = v;
       }
+    } else if (s >= 1 && t - npairs * 64 < s * 128) {
+      // block row s of M, first half, with the threads the update leaves idle
+      const int g = t - npairs * 64;
+      inverse_rows_sum(s, g >> 7, g & 127, Ls, Mt, Tm);
     }
     __syncthreads();
   }
-  // ---- inverse of each diagonal sub-block: lane i computes row i of M_ww
-  if (warp < nsub) {
-    const int w0 = 32 * warp;
-    float acc[32], y[32];
-#pragma unroll
-    for (int c = 0; c < 32; ++c) acc[c] = (c == lane) ? 1.f : 0.f;
-#pragma unroll
-    for (int m = 31; m >= 0; --m) {
-      const float ym = (m <= lane) ? acc[m] * rdiag[w0 + m] : 0.f;
-      y[m] = ym;
-#pragma unroll
-      for (int c = 0; c < m; ++c) acc[c] = fmaf(-ym, Ls[(w0 + m) * LDM + w0 + c], acc[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < 32; ++c) Mt[(w0 + c) * LDM + w0 + lane] = y[c];
-  }
+  // the last block row of M, second half
+  if (nsub >= 2 && t < (nsub - 1) * 128) inverse_rows_finish(nsub - 1, t >> 7, t & 127, Tm, Mt);
   __syncthreads();
-  // ---- sub-blocks below the diagonal of L^-1, one level t - s at a time
-  for (int lv = 1; lv < nsub; ++lv) {
-    const int npair = nsub - lv;
-    const int p = t >> 7, i = t & 31, cg8 = ((t >> 5) & 3) * 8;
-    const int sb = p, tb = p + lv;
-    if (p < npair) {
-      // Tm[p] = sum_{u=sb}^{tb-1} L_{tb,u} M_{u,sb}
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int u = sb; u < tb; ++u) {
-        const float* li = Ls + (32 * tb + i) * LDM + 32 * u;
-#pragma unroll 2
-        for (int m = 0; m < 32; m += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(li + m);
-#pragma unroll
-          for (int cc = 0; cc < 8; ++cc) {
-            const float4 y = *reinterpret_cast<const float4*>(Mt + (32 * sb + cg8 + cc) * LDM + 32 * u + m);
-            acc[cc] = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc[cc]))));
-          }
-        }
-      }
-      float* tm = Tm + (p * 32 + i) * TMLD + cg8;
-      *reinterpret_cast<float4*>(tm) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(tm + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
-    __syncthreads();
-    if (p < npair) {
-      // M_{tb,sb} = -M_{tb,tb} Tm[p]
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int m = 0; m < 32; ++m) {
-        const float mv = Mt[(32 * tb + m) * LDM + 32 * tb + i];
-        const float4 y0 = *reinterpret_cast<const float4*>(Tm + (p * 32 + m) * TMLD + cg8);
-        const float4 y1 = *reinterpret_cast<const float4*>(Tm + (p * 32 + m) * TMLD + cg8 + 4);
-        acc[0] = fmaf(mv, y0.x, acc[0]);
-        acc[1] = fmaf(mv, y0.y, acc[1]);
-        acc[2] = fmaf(mv, y0.z, acc[2]);
-        acc[3] = fmaf(mv, y0.w, acc[3]);
-        acc[4] = fmaf(mv, y1.x, acc[4]);
-        acc[5] = fmaf(mv, y1.y, acc[5]);
-        acc[6] = fmaf(mv, y1.z, acc[6]);
-        acc[7] = fmaf(mv, y1.w, acc[7]);
-      }
-#pragma unroll
-      for (int cc = 0; cc < 8; ++cc) Mt[(32 * sb + cg8 + cc) * LDM + 32 * tb + i] = -acc[cc];
-    }
-    __syncthreads();
-  }
   return bad;
 }
 
@@ -541,9 +556,9 @@ __global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* Ls = Mt + NB * LDM;         // [NB][LDM]  diagonal block, then L_kk
   float* rdiag = Ls + NB * LDM;      // [NB]       1 / diag(L_kk)
-  float* Tm = rdiag + NB;            // [3][32][TMLD] level products
-  float* LT = Tm;                    // [32][LDM] transposed sub-panel (shares Tm's space)
-  float* colbuf = LT + 32 * LDM;     // [2][32]
+  float* LT = rdiag + NB;            // [32][LDM] transposed sub-panel
+  float* Tm = LT + 32 * LDM;         // [3][32][TMLD] partial sums of block rows of M
+  float* colbuf = Tm + 3 * 32 * TMLD;  // [2][32]
   float* LssT = colbuf + 64;         // [32][LST] transposed diagonal sub-block
   const int t = threadIdx.x;
   for (int q = t; q < NB * (NB / 4); q += PT)
@@ -736,7 +751,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     prep_diag_kernel<<<(d + 255) / 256, 256, 0, st>>>(S, diag, perm, d, hscale, lam, Z, zlo, status);
     GPTQ_LAUNCH_CHECK();
   }
-  const size_t smem_factor = sizeof(float) * (2 * NB * LDM + NB + 32 * LDM + 64 + 32 * LST);
+  const size_t smem_factor = sizeof(float) * (2 * NB * LDM + NB + 32 * LDM + 3 * 32 * TMLD + 64 + 32 * LST);
   const size_t smem_role = sizeof(float) * (2 * NB * LDM);
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem_factor)));
