@@ -31,7 +31,9 @@
 // Cost ~ 2 d^3 / 3 flop, all of it in the tensor-core GEMMs except O(d nb^2).
 #include <algorithm>
 
+#include <map>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -682,10 +684,11 @@ size_t prep_workspace_bytes(int64_t d) { return prep_layout(d).total; }
 namespace {
 
 // A second stream with two events, on which one step's update GEMM runs
-// beside the next step's factorization.  Kept in a per-device pool: a call
-// takes one for the time it enqueues its work and puts it back, so calls
-// from several host threads never share one at the same time (a later call
-// that gets the same stream only queues behind the earlier call's work).
+// beside the next step's factorization.  Pooled per (device, caller's
+// stream): a call takes one for the time it enqueues its work and puts it
+// back, so two calls never use the same events at the same time, and calls
+// on different streams (layers solved side by side) get helper streams of
+// their own instead of queueing their hidden GEMMs behind each other.
 struct Helper {
   cudaStream_t stream = nullptr;
   cudaEvent_t ev_pri = nullptr;   // recorded on the caller's stream: step ready for its rest GEMM
@@ -693,14 +696,15 @@ struct Helper {
 };
 
 std::mutex g_helper_mu;
-std::vector<Helper> g_helpers[64];
+std::map<std::pair<int, cudaStream_t>, std::vector<Helper>> g_helpers;
 
-bool take_helper(int dev, Helper& h) {
+bool take_helper(int dev, cudaStream_t caller, Helper& h) {
   {
     std::lock_guard<std::mutex> lock(g_helper_mu);
-    if (!g_helpers[dev].empty()) {
-      h = g_helpers[dev].back();
-      g_helpers[dev].pop_back();
+    auto& pool = g_helpers[{dev, caller}];
+    if (!pool.empty()) {
+      h = pool.back();
+      pool.pop_back();
       return true;
     }
   }
@@ -714,9 +718,9 @@ bool take_helper(int dev, Helper& h) {
   return true;
 }
 
-void give_helper(int dev, const Helper& h) {
+void give_helper(int dev, cudaStream_t caller, const Helper& h) {
   std::lock_guard<std::mutex> lock(g_helper_mu);
-  g_helpers[dev].push_back(h);
+  g_helpers[{dev, caller}].push_back(h);
 }
 
 }  // namespace
@@ -772,7 +776,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   Helper h;
   int dev = 0;
   GPTQ_CUDA_TRY(cudaGetDevice(&dev));
-  if (overlap && (dev < 0 || dev >= 64 || !take_helper(dev, h))) overlap = false;
+  if (overlap && !take_helper(dev, st, h)) overlap = false;
   gptq_status_t result = GPTQ_OK;
   bool rest_pending = false;  // a rest GEMM is queued on the helper stream
   for (int k = 0; k < d && result == GPTQ_OK; k += NB) {
@@ -855,7 +859,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     // Join: the caller's stream ends after the helper stream's last work.
     if (rest_pending && cudaSuccess != cudaStreamWaitEvent(st, h.ev_rest, 0) && result == GPTQ_OK)
       result = GPTQ_ERR_CUDA;
-    give_helper(dev, h);
+    give_helper(dev, st, h);
   }
   return result;
 }

@@ -367,3 +367,32 @@ extern "C" GPTQ_API int gptq_internal_tgemm(const float* A_hi, const float* A_lo
   return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g, gptq::fault_word_ptr(),
                                    reinterpret_cast<cudaStream_t>(stream));
 }
+
+// Test hook (not part of the public header): the same update restricted to
+// one tile subset (0 all, 1 the first tile row and tile column pri_nt, 2 the
+// others), on at most max_ctas CTAs (0: one per SM).
+extern "C" GPTQ_API int gptq_internal_tgemm_subset(const float* A_hi, const float* A_lo, int64_t lda,
+                                                   const float* B_hi, const float* B_lo, int64_t ldb,
+                                                   int M, int N, int K, float alpha, float beta,
+                                                   float* C, int64_t ldc, int lower, int row_off,
+                                                   int col_off, int subset, int pri_nt, int max_ctas,
+                                                   int* tiles, gptq_stream_t stream) {
+  if (subset < 0 || subset > 2 || pri_nt < 0 || max_ctas < 0) return GPTQ_ERR_INVALID_ARG;
+  gptq::TGemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.alpha = alpha;
+  g.beta = beta;
+  g.C = C;
+  g.ldc = ldc;
+  g.lower = lower;
+  g.row_off = row_off;
+  g.col_off = col_off;
+  g.subset = subset;
+  g.pri_nt = pri_nt;
+  g.max_ctas = max_ctas;
+  if (tiles) *tiles = gptq::tgemm_tile_count(g);
+  return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g, gptq::fault_word_ptr(),
+                                   reinterpret_cast<cudaStream_t>(stream));
+}

@@ -66,6 +66,56 @@ def test_tgemm_3xtf32(lib, M, N, K, lower, row_off):
     assert err < 2e-6, err
 
 
+@pytest.mark.parametrize("M,N,K,lower,row_off,pri_nt,max_ctas", [
+    (3968, 4096, 128, 1, 128, 1, 147),    # prepare step 0 at d = 4096
+    (1920, 4096, 128, 1, 2176, 17, 0),    # a middle step
+    (256, 4096, 128, 1, 3840, 30, 5),     # the last step with a rest subset
+    (700, 900, 64, 0, 0, 3, 0),           # ragged, no triangle
+    (128, 512, 96, 1, 384, 3, 0)])        # one tile row: the rest is empty
+def test_tgemm_tile_subsets_partition_the_update(lib, M, N, K, lower, row_off, pri_nt, max_ctas):
+    """The prepare's update GEMM runs as two launches over complementary tile
+    subsets (the next step's row and column blocks first, then the rest, the
+    latter on fewer CTAs).  Together they must give exactly the single
+    launch's result, every tile once: the same tile arithmetic, bit for bit."""
+    import torch
+    f = lib.gptq_internal_tgemm_subset
+    f.restype = ctypes.c_int
+    vp, i64, i32, fl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    f.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32, i32, fl, fl, vp, i64, i32, i32, i32, i32, i32, i32,
+                  vp, vp]
+    rng = np.random.Generator(np.random.PCG64(M * 7 + N + K))
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    C0 = rng.standard_normal((M, N)).astype(np.float32)
+    Ah, Al = split(A)
+    Bh, Bl = split(B)
+    tAh, tAl, tBh, tBl = (torch.from_numpy(x).cuda() for x in (Ah, Al, Bh, Bl))
+    st = torch.cuda.current_stream().cuda_stream
+    out = {}
+    counts = {}
+    for subsets in ((0,), (1, 2), (2, 1)):
+        C = torch.from_numpy(C0).cuda()
+        for sub in subsets:
+            n = ctypes.c_int(-1)
+            rc = f(tAh.data_ptr(), tAl.data_ptr(), K, tBh.data_ptr(), tBl.data_ptr(), K, M, N, K, -1.0, 1.0,
+                   C.data_ptr(), N, lower, row_off, 0, sub, pri_nt, max_ctas if sub == 2 else 0,
+                   ctypes.byref(n), st)
+            assert rc == 0
+            counts[sub] = n.value
+        torch.cuda.synchronize()
+        out[subsets] = C.cpu().numpy()
+    assert counts[1] + counts[2] == counts[0]
+    assert counts[1] > 0
+    assert np.array_equal(out[(1, 2)], out[(0,)])
+    assert np.array_equal(out[(2, 1)], out[(0,)])
+    # and the single launch is the update itself
+    want = C0.astype(np.float64) - A.astype(np.float64) @ B.astype(np.float64).T
+    if lower:
+        want = np.where(np.arange(N)[None, :] <= np.arange(M)[:, None] + row_off, want, C0)
+    scale = np.abs(A).astype(np.float64) @ np.abs(B).astype(np.float64).T + np.abs(C0)
+    assert np.max(np.abs(out[(0,)] - want) / scale) < 2e-6
+
+
 def test_grid_quotient_equals_ieee_division(lib):
     """The column loop decides codes on maxq * (w / span) with w / span taken
     from the reciprocal plus one exact-residual correction; it must equal
