@@ -462,7 +462,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
 template <int RT>
 __device__ __forceinline__ void role_products(const PanelArgs& p, bool xrole, int tile, int part,
                                               const float* __restrict__ Mt,
-                                              const float* __restrict__ T) {
+                                              const float* __restrict__ T, float* __restrict__ stg) {
   const int n = p.n, k = p.k, b = p.b;
   const int64_t ldz = n;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -490,17 +490,24 @@ __device__ __forceinline__ void role_products(const PanelArgs& p, bool xrole, in
       }
     }
     const int w = min(NB, k - cbase);
+    // B rows cbase + c, columns r: consecutive lanes, consecutive addresses.
+    // The same values go to U row n-1-(k+r), columns n-1-cbase-c, through
+    // shared memory so that consecutive lanes write consecutive columns.
 #pragma unroll
     for (int i = 0; i < RT; ++i) {
       const int r = row0 + lane + 32 * i;
-      if (r >= b) continue;
-      float* urow = p.U + static_cast<int64_t>(n - 1 - (k + r)) * n + (n - 1 - cbase);
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        if (c0 + cc >= w) continue;
-        urow[-(c0 + cc)] = acc[i][cc];
-        store_split(p.Bhi, p.Blo, static_cast<int64_t>(cbase + c0 + cc) * NB + r, acc[i][cc]);
+        stg[(lane + 32 * i) * LDM + c0 + cc] = acc[i][cc];
+        if (r < b && c0 + cc < w)
+          store_split(p.Bhi, p.Blo, static_cast<int64_t>(cbase + c0 + cc) * NB + r, acc[i][cc]);
       }
+    }
+    __syncthreads();
+    const int nr = min(rows, b - row0);
+    for (int idx = threadIdx.x; idx < nr * w; idx += PT) {
+      const int rl = idx / w, c = idx - rl * w;
+      p.U[static_cast<int64_t>(n - 1 - (k + row0 + rl)) * n + (n - 1 - cbase - c)] = stg[rl * LDM + c];
     }
   } else {
     // Mt[q][c] = M[c][q] is zero for q > c, so q stops after this warp's columns.
@@ -584,6 +591,7 @@ __global__ void __launch_bounds__(PT, 1) panel_role_kernel(PanelArgs p) {
   extern __shared__ __align__(16) float sm[];
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* T = Mt + NB * LDM;          // [NB][LDM]  role operand tile
+  float* stg = T + NB * LDM;         // [NB][LDM]  X role: staged output rows
   const int n = p.n, k = p.k, b = p.b;
   const int64_t ldz = n;
   const int t = threadIdx.x;
@@ -596,9 +604,18 @@ __global__ void __launch_bounds__(PT, 1) panel_role_kernel(PanelArgs p) {
   // Z, B and M come from the previous kernels.
   griddep_wait();
   griddep_launch_dependents();
-  for (int q = t; q < NB * (NB / 4); q += PT) {
-    const int c = q / (NB / 4), r4 = (q % (NB / 4)) * 4;
-    cp_async16(Mt + c * LDM + r4, p.Mg + c * NB + r4, true);
+  if (xrole && !diag_cta) {
+    // The X role reads only its own rows of M: Mt[q][row0 .. row0 + rows).
+    const int rows = NB / p.split, row0 = part * rows, n4 = rows / 4;
+    for (int q = t; q < NB * n4; q += PT) {
+      const int c = q / n4, r4 = row0 + (q % n4) * 4;
+      cp_async16(Mt + c * LDM + r4, p.Mg + c * NB + r4, true);
+    }
+  } else {
+    for (int q = t; q < NB * (NB / 4); q += PT) {
+      const int c = q / (NB / 4), r4 = (q % (NB / 4)) * 4;
+      cp_async16(Mt + c * LDM + r4, p.Mg + c * NB + r4, true);
+    }
   }
   if (diag_cta) {
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -638,11 +655,11 @@ __global__ void __launch_bounds__(PT, 1) panel_role_kernel(PanelArgs p) {
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (p.split == 4)
-    role_products<1>(p, xrole, xrole ? tile : ptile, part, Mt, T);
+    role_products<1>(p, xrole, xrole ? tile : ptile, part, Mt, T, stg);
   else if (p.split == 2)
-    role_products<2>(p, xrole, xrole ? tile : ptile, part, Mt, T);
+    role_products<2>(p, xrole, xrole ? tile : ptile, part, Mt, T, stg);
   else
-    role_products<4>(p, xrole, xrole ? tile : ptile, part, Mt, T);
+    role_products<4>(p, xrole, xrole ? tile : ptile, part, Mt, T, stg);
 }
 
 }  // namespace
@@ -756,7 +773,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     GPTQ_LAUNCH_CHECK();
   }
   const size_t smem_factor = sizeof(float) * (2 * NB * LDM + NB + 32 * LDM + 3 * 32 * TMLD + 64 + 32 * LST);
-  const size_t smem_role = sizeof(float) * (2 * NB * LDM);
+  const size_t smem_role = sizeof(float) * (3 * NB * LDM);
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem_factor)));
   GPTQ_CUDA_TRY(cudaFuncSetAttribute(panel_role_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
