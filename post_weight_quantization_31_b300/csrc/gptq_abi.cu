@@ -36,8 +36,7 @@ gptq_status_t launch_diag_sumsq(const void* X, int64_t d, int64_t n_tok, int64_t
                                 double* diag, cudaStream_t st);
 size_t prep_workspace_bytes(int64_t d);
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d, int64_t n_seen, float damp,
-                             bool desc_act, float* U, int32_t* perm, void* ws, bool overlap,
-                             cudaStream_t st);
+                             bool desc_act, float* U, int32_t* perm, void* ws, cudaStream_t st);
 size_t quant_workspace_bytes(int64_t d_row, int64_t d_col);
 gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row, int64_t d_col, const float* U,
                               const int32_t* perm, const gptq_config_t& cfg, uint8_t* codes,
@@ -137,25 +136,6 @@ namespace {
 
 using namespace gptq;
 
-namespace gptq {
-// gptq_prepare_hinv's checks and launch.  `overlap` runs each step's update
-// partly on a second stream of the library's (see launch_prepare); without
-// it every launch goes to `stream`.
-gptq_status_t prepare_hinv_call(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
-                                const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
-                                size_t ws_bytes, bool overlap, gptq_stream_t stream) {
-  if (!S || !U || !perm) return GPTQ_ERR_INVALID_ARG;
-  if (d_col < 32 || d_col % 32 != 0 || d_col > 46336 || n_seen < 1) return GPTQ_ERR_INVALID_ARG;
-  if (!config_ok(cfg, d_col)) return GPTQ_ERR_INVALID_ARG;
-  if (!aligned(S, 16) || !aligned(U, 16) || !aligned(perm, 4) || (diag && !aligned(diag, 8)))
-    return GPTQ_ERR_INVALID_ARG;
-  if (!ws || !aligned(ws, 256) || ws_bytes < prep_workspace_bytes(d_col)) return GPTQ_ERR_WORKSPACE;
-  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return launch_prepare(S, diag, d_col, n_seen, cfg->damp_percent, cfg->desc_act != 0, U, perm, ws,
-                        overlap, st);
-}
-}  // namespace gptq
 
 extern "C" {
 
@@ -190,7 +170,16 @@ size_t gptq_prepare_workspace_size(int64_t d_col) {
 gptq_status_t gptq_prepare_hinv(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
                                 const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
                                 size_t ws_bytes, gptq_stream_t stream) {
-  return gptq::prepare_hinv_call(S, diag, d_col, n_seen, cfg, U, perm, ws, ws_bytes, true, stream);
+  if (!S || !U || !perm) return GPTQ_ERR_INVALID_ARG;
+  if (d_col < 32 || d_col % 32 != 0 || d_col > 46336 || n_seen < 1) return GPTQ_ERR_INVALID_ARG;
+  if (!config_ok(cfg, d_col)) return GPTQ_ERR_INVALID_ARG;
+  if (!aligned(S, 16) || !aligned(U, 16) || !aligned(perm, 4) || (diag && !aligned(diag, 8)))
+    return GPTQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < prep_workspace_bytes(d_col)) return GPTQ_ERR_WORKSPACE;
+  if (!device_ok()) return GPTQ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return launch_prepare(S, diag, d_col, n_seen, cfg->damp_percent, cfg->desc_act != 0, U, perm, ws,
+                        st);
 }
 
 size_t gptq_quantize_workspace_size(int64_t d_row, int64_t d_col, const gptq_config_t* cfg) {

@@ -31,10 +31,6 @@
 // Cost ~ 2 d^3 / 3 flop, all of it in the tensor-core GEMMs except O(d nb^2).
 #include <algorithm>
 
-#include <map>
-#include <mutex>
-#include <utility>
-#include <vector>
 
 #include "common.cuh"
 #include "tgemm.cuh"
@@ -173,6 +169,7 @@ struct PanelArgs {
   const float* zlo;  // [n] low parts of the diagonal of Z
   int split;         // CTAs per role tile (1, 2 or 4)
   float* Mg;         // [NB][NB] (L_kk^-1)^T, from the factor kernel to the role kernel
+  int wait_first;    // factor kernel: wait for the previous kernel before starting
 };
 
 __device__ __forceinline__ void store_split(float* hi, float* lo, int64_t off, float v) {
@@ -306,7 +303,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
   asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  if (t < b) Ls[t * LDM + t] += zlo[k + t];
+  if (t < b) Ls[t * LDM + t] += __ldcg(zlo + k + t);
   __syncthreads();
   bool bad = false;
   for (int s = 0; s < nsub; ++s) {
@@ -572,11 +569,16 @@ __global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
   const int t = threadIdx.x;
   for (int q = t; q < NB * (NB / 4); q += PT)
     *reinterpret_cast<float4*>(Mt + (q / (NB / 4)) * LDM + (q % (NB / 4)) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-  // Launched with programmatic dependent launch: Z comes from the previous
-  // kernels.  The role kernel that follows is let in only at the end: its
-  // CTAs would otherwise sit on SMs, waiting, for the whole factorization,
-  // and keep them from the update GEMM that runs beside it.
-  griddep_wait();
+  // Launched with programmatic dependent launch.  The diagonal block comes
+  // from the priority GEMM, which has completed once the kernel before this
+  // one (the rest GEMM, which reads and writes neither the block nor what
+  // this kernel writes) has let it in: then this kernel runs beside the rest
+  // GEMM and waits for it only at its end (wait_first = 0).  Otherwise it
+  // waits for the previous kernel first.  The role kernel is let in only at
+  // the end, after that wait, so everything after this kernel is ordered
+  // after the rest GEMM too; and its CTAs do not sit on SMs, waiting,
+  // through the factorization.
+  if (p.wait_first) griddep_wait();
   const bool notpd = factor_invert_blocked(p.Z, p.zlo, p.n, p.k, p.b, Mt, Ls, rdiag, Tm, LT, colbuf, LssT);
   if (t == 0 && notpd) atomicOr(p.status, kStatNotPD);
   __syncthreads();
@@ -584,6 +586,7 @@ __global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
     const int c = idx / (NB / 4), r4 = (idx % (NB / 4)) * 4;
     *reinterpret_cast<float4*>(p.Mg + c * NB + r4) = *reinterpret_cast<const float4*>(Mt + c * LDM + r4);
   }
+  griddep_wait();
   griddep_launch_dependents();
 }
 
@@ -698,53 +701,9 @@ static PrepLayout prep_layout(int64_t d) {
 
 size_t prep_workspace_bytes(int64_t d) { return prep_layout(d).total; }
 
-namespace {
-
-// A second stream with two events, on which one step's update GEMM runs
-// beside the next step's factorization.  Pooled per (device, caller's
-// stream): a call takes one for the time it enqueues its work and puts it
-// back, so two calls never use the same events at the same time, and calls
-// on different streams (layers solved side by side) get helper streams of
-// their own instead of queueing their hidden GEMMs behind each other.
-struct Helper {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t ev_pri = nullptr;   // recorded on the caller's stream: step ready for its rest GEMM
-  cudaEvent_t ev_rest = nullptr;  // recorded on the helper stream: rest GEMM done
-};
-
-std::mutex g_helper_mu;
-std::map<std::pair<int, cudaStream_t>, std::vector<Helper>> g_helpers;
-
-bool take_helper(int dev, cudaStream_t caller, Helper& h) {
-  {
-    std::lock_guard<std::mutex> lock(g_helper_mu);
-    auto& pool = g_helpers[{dev, caller}];
-    if (!pool.empty()) {
-      h = pool.back();
-      pool.pop_back();
-      return true;
-    }
-  }
-  if (cudaStreamCreateWithFlags(&h.stream, cudaStreamNonBlocking) != cudaSuccess) return false;
-  if (cudaEventCreateWithFlags(&h.ev_pri, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h.ev_rest, cudaEventDisableTiming) != cudaSuccess) {
-    if (h.ev_pri) cudaEventDestroy(h.ev_pri);
-    cudaStreamDestroy(h.stream);
-    return false;
-  }
-  return true;
-}
-
-void give_helper(int dev, cudaStream_t caller, const Helper& h) {
-  std::lock_guard<std::mutex> lock(g_helper_mu);
-  g_helpers[{dev, caller}].push_back(h);
-}
-
-}  // namespace
-
 gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, int64_t n_seen,
                              float damp, bool desc_act, float* U, int32_t* perm, void* ws,
-                             bool overlap, cudaStream_t st) {
+                             cudaStream_t st) {
   const int d = static_cast<int>(d64);
   const PrepLayout L = prep_layout(d64);
   char* base = static_cast<char*>(ws);
@@ -781,21 +740,15 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   const int sms = sm_count();
 
   // Step k: factor the diagonal block (one CTA), the role products, then the
-  // update of the trailing rows by B_k, split into two launches.  The
-  // "priority" tiles (the next step's diagonal row block and column block)
-  // are all that step k + 1's factorization and role products read, so with
-  // `overlap` only they run before step k + 1 on the caller's stream, and the
-  // "rest" runs on a helper stream beside step k + 1's factor and role
-  // kernels.  Step k + 1's own update touches the rest's tiles, so it waits
-  // for them; its panel operands go to the other of two B buffers, since the
-  // rest of step k still reads the first.  Without `overlap` the same
-  // launches run in the same order on one stream.
-  Helper h;
-  int dev = 0;
-  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
-  if (overlap && !take_helper(dev, st, h)) overlap = false;
+  // update of the trailing rows by B_k in two launches on this stream: the
+  // "priority" tiles (the next step's row block and column block, all that
+  // step k + 1's factor and role kernels read), then the "rest" on all SMs
+  // but one.  Step k + 1's factor kernel starts beside the rest GEMM on the
+  // SM it leaves free (see panel_factor_kernel), and every later kernel is
+  // still ordered after the rest GEMM.  The panel operand B alternates
+  // between two buffers by step parity.
   gptq_status_t result = GPTQ_OK;
-  bool rest_pending = false;  // a rest GEMM is queued on the helper stream
+  bool after_rest = false;  // the last kernel launched is a rest GEMM
   for (int k = 0; k < d && result == GPTQ_OK; k += NB) {
     const int b = std::min(NB, d - k);
     const int par = (k / NB) & 1;
@@ -813,6 +766,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     pa.status = status;
     pa.zlo = zlo;
     pa.Mg = Mg;
+    pa.wait_first = after_rest ? 0 : 1;
     const int n_pan = (d - k - b + NB - 1) / NB;
     const int tiles = pa.n_acc + n_pan;
     pa.split = (4 * tiles < sms) ? 4 : (2 * tiles < sms) ? 2 : 1;
@@ -827,6 +781,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
       result = GPTQ_ERR_CUDA;
       break;
     }
+    after_rest = false;
     if (k + b >= d) break;
     TGemmArgs g;
     g.M = d - k - b;
@@ -843,40 +798,14 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     g.pri_nt = (k + b) / NB;
     const float* Ahi = Bhi + static_cast<int64_t>(k + b) * NB;
     const float* Alo = Blo + static_cast<int64_t>(k + b) * NB;
-    // The priority tiles overwrite tiles that the previous rest GEMM updates.
-    if (rest_pending && cudaSuccess != cudaStreamWaitEvent(st, h.ev_rest, 0)) {
-      result = GPTQ_ERR_CUDA;
-      break;
-    }
     g.subset = 1;
     result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, st);
     if (result != GPTQ_OK) break;
     g.subset = 2;
     if (tgemm_tile_count(g) == 0) continue;
-    if (!overlap) {
-      result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, st);
-      continue;
-    }
-    // Leave an SM for the next step's factorization.
-    g.max_ctas = sms - 1;
-    if (cudaSuccess != cudaEventRecord(h.ev_pri, st) ||
-        cudaSuccess != cudaStreamWaitEvent(h.stream, h.ev_pri, 0)) {
-      result = GPTQ_ERR_CUDA;
-      break;
-    }
-    result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, h.stream);
-    if (result != GPTQ_OK) break;
-    if (cudaSuccess != cudaEventRecord(h.ev_rest, h.stream)) {
-      result = GPTQ_ERR_CUDA;
-      break;
-    }
-    rest_pending = true;
-  }
-  if (overlap) {
-    // Join: the caller's stream ends after the helper stream's last work.
-    if (rest_pending && cudaSuccess != cudaStreamWaitEvent(st, h.ev_rest, 0) && result == GPTQ_OK)
-      result = GPTQ_ERR_CUDA;
-    give_helper(dev, st, h);
+    g.max_ctas = sms - 1;  // the free SM takes the next factor kernel
+    result = launch_tgemm_3xtf32(Ahi, Alo, NB, Bhi, Blo, NB, g, status, st);
+    after_rest = true;
   }
   return result;
 }

@@ -15,9 +15,6 @@ namespace gptq {
 
 size_t prep_workspace_bytes(int64_t d);
 gptq_status_t read_workspace_status(const void* ws, cudaStream_t st);
-gptq_status_t prepare_hinv_call(const float* S, const double* diag, int64_t d_col, int64_t n_seen,
-                                const gptq_config_t* cfg, float* U, int32_t* perm, void* ws,
-                                size_t ws_bytes, bool overlap, gptq_stream_t stream);
 
 namespace {
 
@@ -62,10 +59,8 @@ extern "C" GPTQ_API gptq_status_t gptq_prepare_hinv_noalloc(const float* S, cons
   if (d_col > 0 && gptq::prep_workspace_bytes(d_col) > gptq::kScratchBytes) return GPTQ_ERR_WORKSPACE;
   void* ws = gptq::scratch_address();
   if (!ws) return GPTQ_ERR_CUDA;
-  // Every launch on the caller's stream: no second stream or events are
-  // created for this call.
-  const gptq_status_t s = gptq::prepare_hinv_call(S, diag, d_col, n_seen, cfg, U, perm, ws,
-                                                  gptq::kScratchBytes, false, stream);
+  const gptq_status_t s =
+      gptq_prepare_hinv(S, diag, d_col, n_seen, cfg, U, perm, ws, gptq::kScratchBytes, stream);
   if (s != GPTQ_OK) return s;
   // The status word of the call sits in the library's array, where the
   // caller cannot read it: wait for the call and report it here.
