@@ -127,27 +127,43 @@ __global__ void prep_diag_kernel(const float* __restrict__ S, const double* __re
   if (!isfinite(v)) atomicOr(status, kStatNonFinite);
 }
 
+// One 32 x 32 tile of Z (rows ii, columns j, lower part) per block of
+// 32 x 8 threads, through shared memory: in processing order without
+// act-order the entries S[q(j)][q(ii)] of a tile form a block of S whose
+// rows are contiguous along ii, so the loads run with the lanes along ii and
+// the stores of Z and U with the lanes along j.
 __global__ void prep_gather_kernel(const float* __restrict__ S, const int32_t* __restrict__ perm, int d,
                                    float hscale, float* __restrict__ Z, float* __restrict__ U,
                                    int* __restrict__ status) {
+  __shared__ float t[32][33];
   const int bi = blockIdx.y, bj = blockIdx.x;
   if (bj > bi) return;
-  const int i = bi * 32 + threadIdx.y * 4;
-  const int j = bj * 32 + threadIdx.x;
+  const int i0 = bi * 32, j0 = bj * 32;
+  const int tx = threadIdx.x;
   int bad = 0;
-  if (j < d) {
-    const int qj = perm[d - 1 - j];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int ii = i + r;
-      if (ii >= d || j > ii) continue;
-      const int qi = perm[d - 1 - ii];
-      const int a = max(qi, qj), b = min(qi, qj);
-      if (ii == j) continue;  // the diagonal: prep_diag_kernel
-      const float v = S[static_cast<size_t>(a) * d + b] * hscale;
-      if (!isfinite(v)) bad = 1;
-      Z[static_cast<size_t>(ii) * d + j] = v;
-      if (ii > j) U[static_cast<size_t>(ii) * d + j] = 0.f;
+  {  // t[jj][iix] = (2/n) S[max(q(ii), q(j))][min(q(ii), q(j))], ii = i0 + tx
+    const int ii = i0 + tx;
+    const int qi = ii < d ? perm[d - 1 - ii] : 0;
+    for (int jj = threadIdx.y; jj < 32; jj += blockDim.y) {
+      const int j = j0 + jj;
+      float v = 0.f;
+      if (ii < d && j < ii) {
+        const int qj = perm[d - 1 - j];
+        const int a = max(qi, qj), b = min(qi, qj);
+        v = S[static_cast<size_t>(a) * d + b] * hscale;
+        if (!isfinite(v)) bad = 1;
+      }
+      t[jj][tx] = v;
+    }
+  }
+  __syncthreads();
+  {  // Z[ii][j] and U[ii][j] = 0 for ii > j, lanes along j (the diagonal: prep_diag_kernel)
+    const int j = j0 + tx;
+    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+      const int ii = i0 + r;
+      if (ii >= d || j >= ii) continue;
+      Z[static_cast<size_t>(ii) * d + j] = t[tx][r];
+      U[static_cast<size_t>(ii) * d + j] = 0.f;
     }
   }
   if (bad) atomicOr(status, kStatNonFinite);

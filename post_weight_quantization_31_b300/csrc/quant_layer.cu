@@ -331,9 +331,13 @@ __global__ void __launch_bounds__(CL_THREADS, 2) column_block_kernel(ColumnArgs 
 }
 
 // Ut = U^T split into TF32 hi/lo (32 x 32 tiles through shared memory).
+// The trailing updates read Ut[n][k] only for n > k (the columns right of
+// a block, against its rows), so the tiles of U below its diagonal block
+// (their transposes lie above Ut's diagonal) are skipped.
 __global__ void transpose_split_kernel(const float* __restrict__ U, int d, float* __restrict__ Ut_hi,
                                        float* __restrict__ Ut_lo) {
   __shared__ float t[32][33];
+  if (blockIdx.x < blockIdx.y) return;
   const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += blockDim.y) {
     const int i = by + r, j = bx + threadIdx.x;
