@@ -417,15 +417,13 @@ def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
         solver._copy_streams = copies
     cap = max(int(c.shape[1]) for c in X_chunks)
     cap = (cap + 7) // 8 * 8
-    stage = solver.staging(cap, count=n_copy + 1)
+    # One staging buffer more than there are copy streams lets each copy
+    # stream start its next chunk while the Hessian of its last one runs.
+    stage = solver.staging(cap, count=n_copy + 2)
     ready = [torch.cuda.Event() for _ in stage]
     free = [torch.cuda.Event() for _ in stage]
     used = [False] * len(stage)
     W_dev = solver.w_buffer(W_host.dtype)
-    with torch.cuda.stream(copies[0]):
-        W_dev.copy_(W_host, non_blocking=True)
-    w_ready = torch.cuda.Event()
-    w_ready.record(copies[0])
     for ci, chunk in enumerate(X_chunks):
         if chunk.shape[0] != d_col or chunk.dtype != torch.float16:
             raise ValueError("each X chunk must be fp16 [d_col, t]")
@@ -442,6 +440,13 @@ def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
         compute.wait_event(ready[b])
         solver.accumulate(buf)
         free[b].record(compute)
+    # W is needed only by the quantize step: its copy goes last, beside the
+    # Hessian of the last chunk and the prepare step.
+    wcs = copies[len(X_chunks) % n_copy]
+    with torch.cuda.stream(wcs):
+        W_dev.copy_(W_host, non_blocking=True)
+    w_ready = torch.cuda.Event()
+    w_ready.record(wcs)
     compute.wait_event(w_ready)
     solver.prepare()
     solver.quantize(W_dev)

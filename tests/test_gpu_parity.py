@@ -91,7 +91,10 @@ def test_hessian_accumulates_over_chunks_and_strides():
 
 
 # ------------------------------------------------------------------ a2
-@pytest.mark.parametrize("d_col,desc_act", [(512, False), (544, True), (1024, True), (2080, False)])
+@pytest.mark.parametrize("d_col,desc_act", [(512, False), (544, True), (1024, True), (2080, False),
+                                             # one step with no update GEMM; a second step of
+                                             # 32 columns, whose update has no rest tiles
+                                             (32, False), (128, True), (160, True)])
 def test_prepare_matches_oracle(d_col, desc_act):
     import torch
     from post_weight_quantization_31_b300 import api
