@@ -1,12 +1,15 @@
 // 3xTF32 GEMM on tcgen05 (see tgemm.cuh for the contract).
 //
-// Structure (one CTA per SM, persistent over output tiles):
-//   warp 0      TMA producer: per 32-wide K slab, four 128 x 32 fp32 tiles
-//               (A_hi, A_lo, B_hi, B_lo) into a 3-stage ring, 128-byte swizzle
+// Structure (one CTA per SM, persistent over output tiles of 128 x BN,
+// BN = 128, or 64 for launches that would fill fewer than half the SMs: the
+// tiles then halve and the CTAs double, and each tile's latency shrinks):
+//   warp 0      TMA producer: per 32-wide K slab, the fp32 tiles A_hi, A_lo
+//               (128 x 32) and B_hi, B_lo (BN x 32) into a 3-stage (BN = 128)
+//               or 4-stage (BN = 64) ring, 128-byte swizzle
 //   warp 1      MMA issuer: per K slab, 4 steps of K=8, each three
 //               tcgen05.mma kind::tf32 (lo*hi, hi*lo, hi*hi) into TMEM
 //   warps 2-9   epilogue: TMEM -> registers -> C = alpha*acc + beta*C
-// Two 128-column TMEM accumulators let the epilogue of one tile overlap the
+// Two BN-column TMEM accumulators let the epilogue of one tile overlap the
 // MMAs of the next.
 #include <algorithm>
 
@@ -19,21 +22,27 @@ namespace gptq {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
 constexpr int BK = 32;  // fp32: 128 bytes per row = one swizzle span
 constexpr int UK = 8;   // K of one kind::tf32 MMA
-constexpr int STAGES = 3;
-constexpr int TILE_BYTES = BM * BK * 4;  // 16 KB (BN == BM)
-constexpr int STAGE_BYTES = 4 * TILE_BYTES;
+constexpr int A_TILE = BM * BK * 4;  // 16 KB
 constexpr int NUM_THREADS = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
-constexpr uint32_t TMEM_COLS = 256;
+
+template <int BN>
+struct TCfg {
+  static constexpr int STAGES = BN == 64 ? 4 : 3;
+  static constexpr int B_TILE = BN * BK * 4;
+  static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int PR = 128 / BN;  // tiles of one 128-column priority block
+};
 
 struct TGemmSched {
   int m_tiles, n_tiles, k_blocks, tiles;
 };
 
 // Tiles of tile row mt below or on the diagonal (all of them without `lower`).
+template <int BN>
 __host__ __device__ __forceinline__ int row_tiles(const TGemmArgs& a, int n_tiles, int mt) {
   if (!a.lower) return n_tiles;
   const long long lim = static_cast<long long>(a.row_off) + static_cast<long long>(mt) * BM + BM - 1 -
@@ -42,35 +51,51 @@ __host__ __device__ __forceinline__ int row_tiles(const TGemmArgs& a, int n_tile
   return static_cast<int>(lim / BN + 1 < n_tiles ? lim / BN + 1 : n_tiles);
 }
 
+// Tiles of row mt inside the priority block of columns [128 pri_nt, + 128).
+template <int BN>
+__host__ __device__ __forceinline__ int pri_tiles(const TGemmArgs& a, int c) {
+  const int lo = a.pri_nt * TCfg<BN>::PR;
+  const int n = c - lo;
+  return n <= 0 ? 0 : (n < TCfg<BN>::PR ? n : TCfg<BN>::PR);
+}
+
 // Tiles of row mt in the launch's subset.
+template <int BN>
 __host__ __device__ __forceinline__ int subset_row_tiles(const TGemmArgs& a, int n_tiles, int mt) {
-  const int c = row_tiles(a, n_tiles, mt);
+  const int c = row_tiles<BN>(a, n_tiles, mt);
   if (a.subset == 0) return c;
-  const int has_pri = (a.pri_nt < c) ? 1 : 0;
-  if (a.subset == 1) return mt == 0 ? c : has_pri;
-  return mt == 0 ? 0 : c - has_pri;
+  const int np = pri_tiles<BN>(a, c);
+  if (a.subset == 1) return mt == 0 ? c : np;
+  return mt == 0 ? 0 : c - np;
 }
 
 // The t-th tile of the subset, rows in order, columns in order within a row.
+template <int BN>
 __device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
                                             int& nt) {
   for (mt = 0; mt < s.m_tiles; ++mt) {
-    const int c = subset_row_tiles(a, s.n_tiles, mt);
+    const int c = subset_row_tiles<BN>(a, s.n_tiles, mt);
     if (t < c) break;
     t -= c;
   }
+  const int lo = a.pri_nt * TCfg<BN>::PR;
   if (a.subset == 1 && mt > 0)
-    nt = a.pri_nt;
-  else if (a.subset == 2 && t >= a.pri_nt)
-    nt = t + 1;
+    nt = lo + t;
+  else if (a.subset == 2 && mt > 0 && t >= lo)
+    nt = t + pri_tiles<BN>(a, row_tiles<BN>(a, s.n_tiles, mt));
   else
     nt = t;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tgemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
                  const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
                  TGemmArgs a, TGemmSched s, int* fault) {
+  constexpr int STAGES = TCfg<BN>::STAGES;
+  constexpr int STAGE_BYTES = TCfg<BN>::STAGE_BYTES;
+  constexpr int B_TILE = TCfg<BN>::B_TILE;
+  constexpr uint32_t TMEM_COLS = TCfg<BN>::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -121,7 +146,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < s.tiles; t += gridDim.x) {
         int mt, nt;
-        tile_coords(a, s, t, mt, nt);
+        tile_coords<BN>(a, s, t, mt, nt);
         for (int kb = 0; kb < s.k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault)) {
             ok = false;
@@ -130,10 +155,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(sa + 0 * TILE_BYTES, &tm_ahi, fb, kb * BK, mt * BM);
-          tma_load_2d(sa + 1 * TILE_BYTES, &tm_alo, fb, kb * BK, mt * BM);
-          tma_load_2d(sa + 2 * TILE_BYTES, &tm_bhi, fb, kb * BK, nt * BN);
-          tma_load_2d(sa + 3 * TILE_BYTES, &tm_blo, fb, kb * BK, nt * BN);
+          tma_load_2d(sa, &tm_ahi, fb, kb * BK, mt * BM);
+          tma_load_2d(sa + A_TILE, &tm_alo, fb, kb * BK, mt * BM);
+          tma_load_2d(sa + 2 * A_TILE, &tm_bhi, fb, kb * BK, nt * BN);
+          tma_load_2d(sa + 2 * A_TILE + B_TILE, &tm_blo, fb, kb * BK, nt * BN);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -160,10 +185,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint64_t d_ahi = smem_desc_sw128_kmajor(sa + 0 * TILE_BYTES);
-          const uint64_t d_alo = smem_desc_sw128_kmajor(sa + 1 * TILE_BYTES);
-          const uint64_t d_bhi = smem_desc_sw128_kmajor(sa + 2 * TILE_BYTES);
-          const uint64_t d_blo = smem_desc_sw128_kmajor(sa + 3 * TILE_BYTES);
+          const uint64_t d_ahi = smem_desc_sw128_kmajor(sa);
+          const uint64_t d_alo = smem_desc_sw128_kmajor(sa + A_TILE);
+          const uint64_t d_bhi = smem_desc_sw128_kmajor(sa + 2 * A_TILE);
+          const uint64_t d_blo = smem_desc_sw128_kmajor(sa + 2 * A_TILE + B_TILE);
 #pragma unroll
           for (int k = 0; k < BK / UK; ++k) {
             const uint64_t off = static_cast<uint64_t>((k * UK * 4) >> 4);  // 32 bytes per step
@@ -198,40 +223,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < s.tiles; t += gridDim.x) {
       int mt, nt;
-      tile_coords(a, s, t, mt, nt);
+      tile_coords<BN>(a, s, t, mt, nt);
       const int m = mt * BM + q * 32 + lane;
       const bool row_ok = m < a.M;
       const long long diag = static_cast<long long>(a.row_off) + m - a.col_off;  // n <= diag
       float* crow = a.C + static_cast<int64_t>(m) * a.ldc;
-      float4 cpre[2][8];
-      bool fast[2];
+      constexpr int NCH = BN / 64;    // 32-column chunks of this warp's half of the tile
+      // Every C value the chunk will update (and the diagonal one, for the
+      // two-sum) is loaded here, before the wait: the loads of a chunk that
+      // the diagonal or the matrix edge cuts are scalar but just as early,
+      // instead of one dependent load-store pair per element after it.
+      const bool need_c = a.beta != 0.f || a.diag_lo != nullptr;
+      float cpre[NCH][32];
+      bool fast[NCH];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int n0 = nt * BN + h * 64 + cc * 32;
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int n0 = nt * BN + h * (BN / 2) + cc * 32;
         fast[cc] = row_ok && (n0 + 32 <= a.N) && (!a.lower || n0 + 31 <= diag) && (a.ldc % 4 == 0);
+        if (fast[cc]) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          cpre[cc][i] = (fast[cc] && a.beta != 0.f)
-                            ? *reinterpret_cast<const float4*>(crow + n0 + 4 * i)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < 8; ++i) {
+            const float4 x = need_c ? *reinterpret_cast<const float4*>(crow + n0 + 4 * i)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            cpre[cc][4 * i] = x.x;
+            cpre[cc][4 * i + 1] = x.y;
+            cpre[cc][4 * i + 2] = x.z;
+            cpre[cc][4 * i + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int n = n0 + i;
+            const bool ok = need_c && row_ok && n < a.N && (!a.lower || n <= diag);
+            cpre[cc][i] = ok ? crow[n] : 0.f;
+          }
+        }
       }
       if (!mbar_wait_bounded(accf_bar(acc), acc_phase, fault)) break;
       tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int n0 = nt * BN + h * 64 + cc * 32;
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int n0 = nt * BN + h * (BN / 2) + cc * 32;
         if (n0 < a.N) {  // warp-uniform
         float v[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                               static_cast<uint32_t>(acc * BN + h * 64 + cc * 32),
+                               static_cast<uint32_t>(acc * BN + h * (BN / 2) + cc * 32),
                            v);
         if (row_ok && a.diag_lo && diag >= n0 && diag < n0 + 32 && diag < a.N) {
           // the diagonal element of this row lies in the chunk: two-sum
           const int i = static_cast<int>(diag - n0);
-          float vi = 0.f;  // v[i] without a dynamic index (keeps v in registers)
+          float vi = 0.f, cv = 0.f;  // v[i], C[diag] without a dynamic index (keeps them in registers)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) vi = (e == i) ? v[e] : vi;
-          const float cv = crow[diag];
+          for (int e = 0; e < 32; ++e) {
+            vi = (e == i) ? v[e] : vi;
+            cv = (e == i) ? cpre[cc][e] : cv;
+          }
           const float tt = -vi;
           const float sum = cv + tt;
           const float bb = sum - cv;
@@ -244,10 +290,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float4 o = make_float4(a.alpha * v[4 * i], a.alpha * v[4 * i + 1], a.alpha * v[4 * i + 2],
                                    a.alpha * v[4 * i + 3]);
             if (a.beta != 0.f) {
-              o.x = fmaf(a.beta, cpre[cc][i].x, o.x);
-              o.y = fmaf(a.beta, cpre[cc][i].y, o.y);
-              o.z = fmaf(a.beta, cpre[cc][i].z, o.z);
-              o.w = fmaf(a.beta, cpre[cc][i].w, o.w);
+              o.x = fmaf(a.beta, cpre[cc][4 * i], o.x);
+              o.y = fmaf(a.beta, cpre[cc][4 * i + 1], o.y);
+              o.z = fmaf(a.beta, cpre[cc][4 * i + 2], o.z);
+              o.w = fmaf(a.beta, cpre[cc][4 * i + 3], o.w);
             }
             *reinterpret_cast<float4*>(crow + n0 + 4 * i) = o;
           }
@@ -257,7 +303,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int n = n0 + i;
             if (n >= a.N || (a.lower && n > diag)) continue;
             float o = a.alpha * v[i];
-            if (a.beta != 0.f) o = fmaf(a.beta, crow[n], o);
+            if (a.beta != 0.f) o = fmaf(a.beta, cpre[cc][i], o);
             crow[n] = o;
           }
         }
@@ -291,57 +337,67 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_f32_map(CUtensorMap* m, const float* base, int64_t rows, int64_t k, int64_t ld) {
+bool make_f32_map(CUtensorMap* m, const float* base, int64_t rows, int64_t k, int64_t ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4};
-  cuuint32_t box[2] = {BK, 128};
+  cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int BN>
 TGemmSched make_sched(const TGemmArgs& a) {
   TGemmSched s;
   s.m_tiles = (a.M + BM - 1) / BM;
   s.n_tiles = (a.N + BN - 1) / BN;
   s.k_blocks = (a.K + BK - 1) / BK;
   s.tiles = 0;
-  for (int mt = 0; mt < s.m_tiles; ++mt) s.tiles += subset_row_tiles(a, s.n_tiles, mt);
+  for (int mt = 0; mt < s.m_tiles; ++mt) s.tiles += subset_row_tiles<BN>(a, s.n_tiles, mt);
   return s;
+}
+
+template <int BN>
+gptq_status_t launch_bn(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
+                        const float* B_lo, int64_t ldb, const TGemmArgs& args, const TGemmSched& s,
+                        int* fault, cudaStream_t st) {
+  CUtensorMap m_ahi, m_alo, m_bhi, m_blo;
+  if (!make_f32_map(&m_ahi, A_hi, args.M, args.K, lda, BM) ||
+      !make_f32_map(&m_alo, A_lo, args.M, args.K, lda, BM) ||
+      !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb, BN) ||
+      !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb, BN))
+    return GPTQ_ERR_CUDA;
+  GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TCfg<BN>::SMEM_BYTES));
+  int grid = std::min(sm_count(), s.tiles);
+  if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
+  GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel<BN>, dim3(grid), dim3(NUM_THREADS), TCfg<BN>::SMEM_BYTES, st,
+                           m_ahi, m_alo, m_bhi, m_blo, args, s, fault));
+  GPTQ_LAUNCH_CHECK();
+  return GPTQ_OK;
 }
 
 }  // namespace
 
-int tgemm_tile_count(const TGemmArgs& args) { return make_sched(args).tiles; }
+int tgemm_tile_count(const TGemmArgs& args) { return make_sched<128>(args).tiles; }
 
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
                                   const float* B_lo, int64_t ldb, const TGemmArgs& args, int* fault,
                                   cudaStream_t st) {
   if (!fault) return GPTQ_ERR_CUDA;
   if (args.M <= 0 || args.N <= 0 || args.K <= 0) return GPTQ_OK;
-  const TGemmSched s = make_sched(args);
+  const TGemmSched s = make_sched<128>(args);
   if (s.tiles == 0) return GPTQ_OK;
-  CUtensorMap m_ahi, m_alo, m_bhi, m_blo;
-  if (!make_f32_map(&m_ahi, A_hi, args.M, args.K, lda) || !make_f32_map(&m_alo, A_lo, args.M, args.K, lda) ||
-      !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb) || !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb))
-    return GPTQ_ERR_CUDA;
-  static int attr_dev = -1;
-  int dev = 0;
-  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
-  if (attr_dev != dev) {
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       SMEM_BYTES));
-    attr_dev = dev;
+  // A launch that would fill fewer than half the SMs runs 128 x 64 tiles:
+  // twice the CTAs, each tile's loads, MMAs and epilogue about half.
+  if (2 * s.tiles <= sm_count()) {
+    const TGemmSched s64 = make_sched<64>(args);
+    return launch_bn<64>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s64, fault, st);
   }
-  int grid = std::min(sm_count(), s.tiles);
-  if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
-  GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, st, m_ahi, m_alo,
-                           m_bhi, m_blo, args, s, fault));
-  GPTQ_LAUNCH_CHECK();
-  return GPTQ_OK;
+  return launch_bn<128>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s, fault, st);
 }
 
 }  // namespace gptq
