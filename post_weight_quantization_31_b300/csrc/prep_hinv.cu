@@ -27,10 +27,11 @@
 //                  where B = [X_k^T ; P] (hi/lo TF32 split) is n x 128;
 //   update GEMM    Z[>k rows, :] (lower) -= P B^T  on the tensor cores (3xTF32):
 //                  the columns left of the diagonal get the Acc update
-//                  (-P X_k), the rest the Schur update (-P P^T).
+//                  (-P X_k), the rest the Schur update (-P P^T); first the
+//                  tiles step k + 1 reads, then the rest, beside the factor
+//                  kernel of step k + 1 (see launch_prepare).
 // Cost ~ 2 d^3 / 3 flop, all of it in the tensor-core GEMMs except O(d nb^2).
 #include <algorithm>
-
 
 #include "common.cuh"
 #include "tgemm.cuh"

@@ -32,8 +32,10 @@ struct TGemmArgs {
   // C + diag_lo carries the running diagonal to about twice fp32 precision.
   float* diag_lo = nullptr;
   // Optional tile subsets, for splitting one update into two launches:
-  // subset 1 takes the tiles of the first tile row (mt == 0) and of tile
-  // column pri_nt; subset 2 takes all the others; 0 takes every tile.
+  // subset 1 takes the tiles of the first 128 rows (tile row 0) and of the
+  // 128 columns [128 pri_nt, 128 pri_nt + 128); subset 2 takes all the
+  // others; 0 takes every tile.  The two subsets together are the whole
+  // update, each element computed exactly as the single launch computes it.
   int subset = 0;
   int pri_nt = 0;
   // At most this many CTAs (0: one per SM).
@@ -60,8 +62,9 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
                                   const float* B_hi, const float* B_lo, int64_t ldb,
                                   const TGemmArgs& args, int* fault, cudaStream_t st);
 
-// Number of 128 x 128 output tiles the launch above would process (of its
-// subset).
+// Number of 128 x 128 output tiles of the launch's subset (a launch that
+// would fill fewer than half the SMs runs 128 x 64 tiles instead, twice as
+// many).
 int tgemm_tile_count(const TGemmArgs& args);
 
 }  // namespace gptq
