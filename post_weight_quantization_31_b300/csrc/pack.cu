@@ -59,6 +59,66 @@ __global__ void pack_qweight_kernel(const uint8_t* __restrict__ codes, int d_row
   }
 }
 
+// 2, 4 and 8 bits: a word holds whole codes, so each thread packs the 32
+// codes of one row's 32-column chunk (two 16-byte loads, a whole sector)
+// into `bits` words straight from registers; the lanes of a warp take 32
+// consecutive rows, so every word store is one coalesced 128-byte line.
+// The threads after those pack the zero points, one qzeros word each (the
+// same launch, so the small qzeros work adds no launch of its own).
+template <int BITS>
+__global__ void pack_qweight_whole_kernel(const uint8_t* __restrict__ codes, int d_row, int d_col,
+                                          int32_t* __restrict__ qweight,
+                                          const uint8_t* __restrict__ zeros, int n_groups,
+                                          int32_t* __restrict__ qzeros) {
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nq = static_cast<int64_t>(d_row) * (d_col / 32);
+  if (gid >= nq) {
+    const int words = d_row * BITS / 32;
+    const int64_t zid = gid - nq;
+    if (zid >= static_cast<int64_t>(words) * n_groups) return;
+    const int g = static_cast<int>(zid / words), kw = static_cast<int>(zid % words);
+    qzeros[static_cast<size_t>(g) * words + kw] = static_cast<int32_t>(
+        stream_word(zeros + static_cast<size_t>(g) * d_row, 1, kw, BITS, (1u << BITS) - 1u));
+    return;
+  }
+  const int r = static_cast<int>(gid % d_row);
+  const int chunk = static_cast<int>(gid / d_row);
+  const uint4* src = reinterpret_cast<const uint4*>(codes + static_cast<size_t>(r) * d_col + chunk * 32);
+  const uint4 a = src[0], b = src[1];
+  const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};  // 4 codes per word, one per byte
+  int32_t* dst = qweight + static_cast<size_t>(chunk) * BITS * d_row + r;
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[static_cast<size_t>(j) * d_row] = static_cast<int32_t>(u[j]);
+  } else if constexpr (BITS == 4) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // 4 bytes -> 4 nibbles in the low 16 bits
+        uint32_t t = u[2 * j + h] & 0x0F0F0F0Fu;
+        t = (t | (t >> 4)) & 0x00FF00FFu;
+        t = (t | (t >> 8)) & 0x0000FFFFu;
+        w |= t << (16 * h);
+      }
+      dst[static_cast<size_t>(j) * d_row] = static_cast<int32_t>(w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {  // 4 bytes -> 4 two-bit fields in the low 8 bits
+        uint32_t t = u[4 * j + h] & 0x03030303u;
+        t = (t | (t >> 6)) & 0x000F000Fu;
+        t = (t | (t >> 12)) & 0x000000FFu;
+        w |= t << (8 * h);
+      }
+      dst[static_cast<size_t>(j) * d_row] = static_cast<int32_t>(w);
+    }
+  }
+}
+
 __global__ void pack_qzeros_kernel(const uint8_t* __restrict__ zeros, int d_row, int n_groups, int bits,
                                    int32_t* __restrict__ qzeros) {
   const int words = d_row * bits / 32;
@@ -99,6 +159,19 @@ __global__ void unpack_qzeros_kernel(const int32_t* __restrict__ qzeros, int d_r
 
 gptq_status_t launch_pack(const uint8_t* codes, const uint8_t* zeros, int64_t d_row, int64_t d_col,
                           int bits, int n_groups, int32_t* qweight, int32_t* qzeros, cudaStream_t st) {
+  if (bits != 3) {
+    const int64_t threads = d_row * (d_col / 32) + d_row * bits / 32 * n_groups;   // d_col % 32 == 0
+    const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+    const int dr = static_cast<int>(d_row), dc = static_cast<int>(d_col);
+    if (bits == 8)
+      pack_qweight_whole_kernel<8><<<blocks, 256, 0, st>>>(codes, dr, dc, qweight, zeros, n_groups, qzeros);
+    else if (bits == 4)
+      pack_qweight_whole_kernel<4><<<blocks, 256, 0, st>>>(codes, dr, dc, qweight, zeros, n_groups, qzeros);
+    else
+      pack_qweight_whole_kernel<2><<<blocks, 256, 0, st>>>(codes, dr, dc, qweight, zeros, n_groups, qzeros);
+    GPTQ_LAUNCH_CHECK();
+    return GPTQ_OK;
+  }
   dim3 g1((d_col + PK_COLS - 1) / PK_COLS, (d_row + PK_ROWS - 1) / PK_ROWS);
   pack_qweight_kernel<<<g1, 256, 0, st>>>(codes, static_cast<int>(d_row), static_cast<int>(d_col), bits,
                                           qweight);
