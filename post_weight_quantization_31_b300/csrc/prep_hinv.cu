@@ -47,27 +47,32 @@ __device__ __forceinline__ unsigned long long ordered_key(double x) {
 }
 
 // ---------------------------------------------------------------- stats
+// The sort keys of the diagonal, and per block of 256 entries the fp64 sum
+// of the diagonal (`part`, summed in a fixed order by prep_diag_kernel, so
+// that lambda does not depend on the schedule).  Also perm = identity when
+// there is no act-order.
+constexpr int ST_THREADS = 256;
+
 __global__ void prep_stats_kernel(const float* __restrict__ S, const double* __restrict__ diag, int d,
-                                  double hscale, float damp, unsigned long long* __restrict__ keys,
-                                  float* __restrict__ lam_out, int* __restrict__ status) {
-  __shared__ double red[32];
-  double sum = 0.0;
-  int bad = 0;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const double v = diag ? diag[i] : static_cast<double>(S[static_cast<size_t>(i) * d + i]);
-    if (!isfinite(v)) bad = 1;
-    sum += v;
+                                  unsigned long long* __restrict__ keys, double* __restrict__ part,
+                                  int32_t* __restrict__ iota_perm, int* __restrict__ status) {
+  __shared__ double red[ST_THREADS / 32];
+  const int i = blockIdx.x * ST_THREADS + threadIdx.x;
+  double v = 0.0;
+  if (i < d) {
+    v = diag ? diag[i] : static_cast<double>(S[static_cast<size_t>(i) * d + i]);
+    if (!isfinite(v)) atomicOr(status, kStatNonFinite);
     keys[i] = ordered_key(v);
+    if (iota_perm) iota_perm[i] = i;
   }
+  double sum = v;
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sum;
-  if (bad) atomicOr(status, kStatNonFinite);
   __syncthreads();
   if (threadIdx.x == 0) {
     double tot = 0.0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += red[w];
-    // mean(diag H) = (2/n) * mean(diag S)
-    *lam_out = static_cast<float>(static_cast<double>(damp) * hscale * tot / d);
+    for (int w = 0; w < ST_THREADS / 32; ++w) tot += red[w];
+    part[blockIdx.x] = tot;
   }
 }
 
@@ -97,11 +102,6 @@ __global__ void prep_rank_kernel(const unsigned long long* __restrict__ keys, in
   if (i < d) perm[rank] = i;
 }
 
-__global__ void iota_kernel(int32_t* __restrict__ perm, int d) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < d) perm[i] = i;
-}
-
 // ---------------------------------------------------------------- gather
 // prep_diag_kernel: Z[i][i] + zlo[i] = (2/n) S_ii + lambda, formed in fp64 and
 // carried as an fp32 pair (see the update GEMM), S_ii taken from the fp64
@@ -113,15 +113,20 @@ __global__ void iota_kernel(int32_t* __restrict__ perm, int d) {
 // q(i) = perm[d-1-i]; also U[i][j] = 0 for i > j (the part of U the panel
 // steps do not write).
 __global__ void prep_diag_kernel(const float* __restrict__ S, const double* __restrict__ diag,
-                                 const int32_t* __restrict__ perm, int d, double hscale_d,
-                                 const float* __restrict__ lam, float* __restrict__ Z,
+                                 const int32_t* __restrict__ perm, int d, double hscale_d, float damp,
+                                 const double* __restrict__ part, int nparts, float* __restrict__ Z,
                                  float* __restrict__ zlo, int* __restrict__ status) {
+  // lambda = damp * mean(diag H) = damp * (2/n) * mean(diag S), the block sums
+  // added in block order.
+  double tot = 0.0;
+  for (int b = 0; b < nparts; ++b) tot += part[b];
+  const float lam = static_cast<float>(static_cast<double>(damp) * hscale_d * tot / d);
   // The diagonal is carried as Z + zlo (see the update GEMM).
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= d) return;
   const int qi = perm[d - 1 - i];
   const double s = diag ? diag[qi] : static_cast<double>(S[static_cast<size_t>(qi) * d + qi]);
-  const double v64 = s * hscale_d + static_cast<double>(*lam);
+  const double v64 = s * hscale_d + static_cast<double>(lam);
   const float v = static_cast<float>(v64);
   Z[static_cast<size_t>(i) * d + i] = v;
   zlo[i] = static_cast<float>(v64 - static_cast<double>(v));
@@ -686,7 +691,7 @@ __global__ void __launch_bounds__(PT, 1) panel_role_kernel(PanelArgs p) {
 
 // Workspace layout (byte offsets, each 256-aligned).
 struct PrepLayout {
-  size_t status, lam, keys, zlo, Z, Mg, Bhi[2], Blo[2], total;
+  size_t status, part, keys, zlo, Z, Mg, Bhi[2], Blo[2], total;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -696,8 +701,8 @@ static PrepLayout prep_layout(int64_t d) {
   size_t off = 0;
   L.status = off;
   off += 256;
-  L.lam = off;
-  off += 256;
+  L.part = off;  // fp64 sums of the diagonal, one per 256 entries
+  off = align256(off + sizeof(double) * ((d + ST_THREADS - 1) / ST_THREADS));
   L.keys = off;
   off = align256(off + sizeof(unsigned long long) * d);
   L.zlo = off;
@@ -725,7 +730,8 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   const PrepLayout L = prep_layout(d64);
   char* base = static_cast<char*>(ws);
   int* status = reinterpret_cast<int*>(base + L.status);
-  float* lam = reinterpret_cast<float*>(base + L.lam);
+  double* part = reinterpret_cast<double*>(base + L.part);
+  const int nparts = (d + ST_THREADS - 1) / ST_THREADS;
   auto* keys = reinterpret_cast<unsigned long long*>(base + L.keys);
   float* Z = reinterpret_cast<float*>(base + L.Z);
   float* zlo = reinterpret_cast<float*>(base + L.zlo);
@@ -733,19 +739,19 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
   const double hscale = 2.0 / static_cast<double>(n_seen);
 
   GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
-  prep_stats_kernel<<<1, 1024, 0, st>>>(S, diag, d, hscale, damp, keys, lam, status);
+  prep_stats_kernel<<<nparts, ST_THREADS, 0, st>>>(S, diag, d, keys, part, desc_act ? nullptr : perm,
+                                                   status);
   GPTQ_LAUNCH_CHECK();
   if (desc_act) {
     prep_rank_kernel<<<(d + 255) / 256, 256, 0, st>>>(keys, d, perm);
-  } else {
-    iota_kernel<<<(d + 255) / 256, 256, 0, st>>>(perm, d);
+    GPTQ_LAUNCH_CHECK();
   }
-  GPTQ_LAUNCH_CHECK();
   {
     dim3 grid((d + 31) / 32, (d + 31) / 32), block(32, 8);
     prep_gather_kernel<<<grid, block, 0, st>>>(S, perm, d, static_cast<float>(hscale), Z, U, status);
     GPTQ_LAUNCH_CHECK();
-    prep_diag_kernel<<<(d + 255) / 256, 256, 0, st>>>(S, diag, perm, d, hscale, lam, Z, zlo, status);
+    prep_diag_kernel<<<(d + 255) / 256, 256, 0, st>>>(S, diag, perm, d, hscale, damp, part, nparts, Z, zlo,
+                                                      status);
     GPTQ_LAUNCH_CHECK();
   }
   const size_t smem_factor = sizeof(float) * (2 * NB * LDM + NB + 32 * LDM + 3 * 32 * TMLD + 64 + 32 * LST);

@@ -20,12 +20,13 @@ namespace {
 
 constexpr int64_t kMaxDCol = GPTQ_NOALLOC_MAX_D_COL;
 constexpr size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
-// Room for the prepare workspace at d_col = kMaxDCol: status and damping
-// words, the 64-bit sort keys, the low parts of the work matrix's diagonal,
-// the d x d work matrix, the 128 x 128 inverse of a diagonal block, and two
-// pairs of d x 128 panel operands.  Each call checks it against
-// prep_workspace_bytes().
-constexpr size_t kScratchBytes = 256 + 256 + round256(8 * kMaxDCol) + round256(4 * kMaxDCol) +
+// Room for the prepare workspace at d_col = kMaxDCol: the status word, the
+// per-block sums of the diagonal, the 64-bit sort keys, the low parts of the
+// work matrix's diagonal, the d x d work matrix, the 128 x 128 inverse of a
+// diagonal block, and two pairs of d x 128 panel operands.  Each call checks
+// it against prep_workspace_bytes().
+constexpr size_t kScratchBytes = 256 + round256(8 * (kMaxDCol / 256 + 1)) + round256(8 * kMaxDCol) +
+                                 round256(4 * kMaxDCol) +
                                  round256(4 * kMaxDCol * kMaxDCol) + round256(4 * 128 * 128) +
                                  4 * round256(4 * kMaxDCol * 128);
 

@@ -122,7 +122,10 @@ __device__ __forceinline__ float to_f32<__half>(__half v) {
   return __half2float(v);
 }
 
-// Wf[r][i] = W[r][perm[i]]; g_idx[perm[i]] = i / gs.
+// Wf[r][i] = W[r][perm[i]]; g_idx[perm[i]] = i / gs.  Each thread takes
+// LW_ROWS rows of one column, all loads issued before the stores.
+constexpr int LW_ROWS = 8;
+
 template <typename T>
 __global__ void load_w_kernel(const T* __restrict__ W, const int32_t* __restrict__ perm, int d_row,
                               int d_col, int gs, float* __restrict__ Wf, int32_t* __restrict__ g_idx,
@@ -132,10 +135,17 @@ __global__ void load_w_kernel(const T* __restrict__ W, const int32_t* __restrict
   const int src = perm[i];
   if (blockIdx.y == 0) g_idx[src] = gs > 0 ? i / gs : 0;
   int bad = 0;
-  for (int r = blockIdx.y; r < d_row; r += gridDim.y) {
-    const float v = to_f32<T>(W[static_cast<size_t>(r) * d_col + src]);
-    if (!isfinite(v)) bad = 1;
-    Wf[static_cast<size_t>(r) * d_col + i] = v;
+  for (int r0 = blockIdx.y * LW_ROWS; r0 < d_row; r0 += gridDim.y * LW_ROWS) {
+    float v[LW_ROWS];
+#pragma unroll
+    for (int j = 0; j < LW_ROWS; ++j)
+      v[j] = r0 + j < d_row ? to_f32<T>(W[static_cast<size_t>(r0 + j) * d_col + src]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < LW_ROWS; ++j) {
+      if (r0 + j >= d_row) break;
+      if (!isfinite(v[j])) bad = 1;
+      Wf[static_cast<size_t>(r0 + j) * d_col + i] = v[j];
+    }
   }
   if (bad) atomicOr(status, kStatNonFinite);
 }
@@ -408,7 +418,7 @@ gptq_status_t launch_quantize(const void* W, int w_dtype, int64_t d_row64, int64
 
   GPTQ_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int), st));
   {
-    dim3 grid((d_col + 255) / 256, std::min(d_row, 64));
+    dim3 grid((d_col + 255) / 256, std::min((d_row + LW_ROWS - 1) / LW_ROWS, 4096));
     if (w_dtype == GPTQ_W_FP32)
       load_w_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(W), perm, d_row, d_col, gs,
                                                  Wf, g_idx, status);
