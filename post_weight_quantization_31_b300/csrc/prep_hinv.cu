@@ -793,11 +793,13 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     const int n_pan = (d - k - b + NB - 1) / NB;
     const int tiles = pa.n_acc + n_pan;
     pa.split = (4 * tiles < sms) ? 4 : (2 * tiles < sms) ? 2 : 1;
+    count_launch();
     if (cudaSuccess != launch_pdl(panel_factor_kernel, dim3(1), dim3(PT), smem_factor, st, pa) ||
         cudaSuccess != cudaGetLastError()) {
       result = GPTQ_ERR_CUDA;
       break;
     }
+    count_launch();
     if (cudaSuccess != launch_pdl(panel_role_kernel, dim3(tiles * pa.split + 1), dim3(PT), smem_role, st,
                                   pa) ||
         cudaSuccess != cudaGetLastError()) {
