@@ -12,6 +12,7 @@
 // Two BN-column TMEM accumulators let the epilogue of one tile overlap the
 // MMAs of the next.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -370,8 +371,17 @@ gptq_status_t launch_bn(const float* A_hi, const float* A_lo, int64_t lda, const
       !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb, BN) ||
       !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb, BN))
     return GPTQ_ERR_CUDA;
-  GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     TCfg<BN>::SMEM_BYTES));
+  // The shared-memory attribute is set once per device (two threads that
+  // race here both set the same value).
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  GPTQ_CUDA_TRY(cudaGetDevice(&dev));
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (!bit || !(attr_set.load(std::memory_order_relaxed) & bit)) {
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TCfg<BN>::SMEM_BYTES));
+    attr_set.fetch_or(bit, std::memory_order_relaxed);
+  }
   int grid = std::min(sm_count(), s.tiles);
   if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
   GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel<BN>, dim3(grid), dim3(NUM_THREADS), TCfg<BN>::SMEM_BYTES, st,
