@@ -60,9 +60,9 @@ constexpr int SB = 4 * CB;         // super-block of the two-level lazy update
 // 4096 x 4096 quantize: 16 lanes 1.334 ms, 8 lanes 1.241 ms, 4 lanes 1.350 ms.
 constexpr int LPR = 8;             // lanes per row
 constexpr int CPL = CB / LPR;      // columns of a row held by one lane (registers)
-constexpr int USEG = CPL + 4;      // padded 8-column segment of a U row in smem
+constexpr int USEG = CPL + 4;      // padded CPL-column segment of a U row in smem
 constexpr int UROW = LPR * USEG;   // padded U row
-constexpr int CL_THREADS = 128;
+constexpr int CL_THREADS = 128;    // 4 warps, 16 rows per CTA, 2 CTAs per SM
 constexpr int CL_ROWS = CL_THREADS / LPR;
 
 struct QParams {
