@@ -88,7 +88,14 @@ __device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched
     nt = t;
 }
 
-template <int BN>
+// PAIR: clusters of two CTAs take the vertically adjacent tiles (2p, nt) and
+// (2p + 1, nt) of a full (non-triangular, all-tiles) update; they share the
+// tile's B rows, so each CTA loads its own A and one half of B, multicast to
+// both (TMA multicast within this GPU's memory): 48 KB of L2 reads per
+// 32-wide K slab and CTA instead of 64 KB.  A slot is free again once both
+// CTAs' MMAs have read it: each MMA thread releases it in both CTAs with one
+// multicast commit.
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tgemm_kernel(const __grid_constant__ CUtensorMap tm_ahi, const __grid_constant__ CUtensorMap tm_alo,
                  const __grid_constant__ CUtensorMap tm_bhi, const __grid_constant__ CUtensorMap tm_blo,
@@ -110,11 +117,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cid = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nclusters = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // the tile of job t: in PAIR mode, pair row block t / n_tiles, column t % n_tiles
+  auto job_tile = [&](int t, int& mt, int& nt) {
+    if constexpr (PAIR) {
+      mt = 2 * (t / s.n_tiles) + rank;
+      nt = t % s.n_tiles;
+    } else {
+      tile_coords<BN>(a, s, t, mt, nt);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), 1);
+      mbar_init(empty_bar(i), PAIR ? 2 : 1);   // PAIR: released by both CTAs' MMAs
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
@@ -132,7 +151,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();   // both CTAs' barriers exist before either multicasts into the other
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above is independent of the previous kernel (launched with
@@ -145,9 +167,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < s.tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < s.tiles; t += nclusters) {
         int mt, nt;
-        tile_coords<BN>(a, s, t, mt, nt);
+        job_tile(t, mt, nt);
         for (int kb = 0; kb < s.k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault)) {
             ok = false;
@@ -158,8 +180,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(sa, &tm_ahi, fb, kb * BK, mt * BM);
           tma_load_2d(sa + A_TILE, &tm_alo, fb, kb * BK, mt * BM);
-          tma_load_2d(sa + 2 * A_TILE, &tm_bhi, fb, kb * BK, nt * BN);
-          tma_load_2d(sa + 2 * A_TILE + B_TILE, &tm_blo, fb, kb * BK, nt * BN);
+          if constexpr (PAIR) {  // own half of B, to both CTAs; the other half comes from the peer
+            tma_load_2d_multicast(sa + 2 * A_TILE + rank * (B_TILE / 2), &tm_bhi, fb, kb * BK,
+                                  nt * BN + rank * (BN / 2), 0x3);
+            tma_load_2d_multicast(sa + 2 * A_TILE + B_TILE + rank * (B_TILE / 2), &tm_blo, fb, kb * BK,
+                                  nt * BN + rank * (BN / 2), 0x3);
+          } else {
+            tma_load_2d(sa + 2 * A_TILE, &tm_bhi, fb, kb * BK, nt * BN);
+            tma_load_2d(sa + 2 * A_TILE + B_TILE, &tm_blo, fb, kb * BK, nt * BN);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if constexpr (PAIR) {
+        // Before this CTA may exit, every release the peer sends to its
+        // slots must have landed: wait for one more turn of the ring.
+        for (int i = 0; i < STAGES; ++i) {
+          mbar_wait_bounded(empty_bar(stage), phase ^ 1u, fault);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -175,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < s.tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < s.tiles; t += nclusters) {
         if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, fault)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -198,7 +238,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_mma_tf32(d_tmem, d_ahi + off, d_blo + off, idesc, 1u);
             tc_mma_tf32(d_tmem, d_ahi + off, d_bhi + off, idesc, 1u);
           }
-          tc_commit(empty_bar(stage));
+          if constexpr (PAIR)
+            tc_commit_multicast(empty_bar(stage), 0x3);  // frees the slot in both CTAs
+          else
+            tc_commit(empty_bar(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -222,9 +265,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int h = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < s.tiles; t += gridDim.x) {
+    for (int t = cid; t < s.tiles; t += nclusters) {
       int mt, nt;
-      tile_coords<BN>(a, s, t, mt, nt);
+      job_tile(t, mt, nt);
       const int m = mt * BM + q * 32 + lane;
       const bool row_ok = m < a.M;
       const long long diag = static_cast<long long>(a.row_off) + m - a.col_off;  // n <= diag
@@ -318,7 +361,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();   // neither CTA leaves while the other may still use its shared memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -361,15 +407,16 @@ TGemmSched make_sched(const TGemmArgs& a) {
   return s;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 gptq_status_t launch_bn(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
                         const float* B_lo, int64_t ldb, const TGemmArgs& args, const TGemmSched& s,
                         int* fault, cudaStream_t st) {
   CUtensorMap m_ahi, m_alo, m_bhi, m_blo;
+  const int b_rows = PAIR ? BN / 2 : BN;   // PAIR: each CTA loads half of B
   if (!make_f32_map(&m_ahi, A_hi, args.M, args.K, lda, BM) ||
       !make_f32_map(&m_alo, A_lo, args.M, args.K, lda, BM) ||
-      !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb, BN) ||
-      !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb, BN))
+      !make_f32_map(&m_bhi, B_hi, args.N, args.K, ldb, b_rows) ||
+      !make_f32_map(&m_blo, B_lo, args.N, args.K, ldb, b_rows))
     return GPTQ_ERR_CUDA;
   // The shared-memory attribute is set once per device (two threads that
   // race here both set the same value).
@@ -378,14 +425,36 @@ gptq_status_t launch_bn(const float* A_hi, const float* A_lo, int64_t lda, const
   GPTQ_CUDA_TRY(cudaGetDevice(&dev));
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (!bit || !(attr_set.load(std::memory_order_relaxed) & bit)) {
-    GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    GPTQ_CUDA_TRY(cudaFuncSetAttribute(tgemm_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TCfg<BN>::SMEM_BYTES));
     attr_set.fetch_or(bit, std::memory_order_relaxed);
   }
-  int grid = std::min(sm_count(), s.tiles);
-  if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
-  GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel<BN>, dim3(grid), dim3(NUM_THREADS), TCfg<BN>::SMEM_BYTES, st,
-                           m_ahi, m_alo, m_bhi, m_blo, args, s, fault));
+  if constexpr (PAIR) {
+    // one cluster of two CTAs per tile pair in flight, launched like launch_pdl
+    int clusters = std::min(sm_count() / 2, s.tiles);
+    if (args.max_ctas > 0) clusters = std::min(clusters, std::max(1, args.max_ctas / 2));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = TCfg<BN>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    GPTQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, tgemm_kernel<BN, PAIR>, m_ahi, m_alo, m_bhi, m_blo, args, s,
+                                     fault));
+  } else {
+    int grid = std::min(sm_count(), s.tiles);
+    if (args.max_ctas > 0) grid = std::min(grid, args.max_ctas);
+    GPTQ_CUDA_TRY(launch_pdl(tgemm_kernel<BN, PAIR>, dim3(grid), dim3(NUM_THREADS), TCfg<BN>::SMEM_BYTES,
+                             st, m_ahi, m_alo, m_bhi, m_blo, args, s, fault));
+  }
   GPTQ_LAUNCH_CHECK();
   return GPTQ_OK;
 }
@@ -405,9 +474,17 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
   // twice the CTAs, each tile's loads, MMAs and epilogue about half.
   if (2 * s.tiles <= sm_count()) {
     const TGemmSched s64 = make_sched<64>(args);
-    return launch_bn<64>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s64, fault, st);
+    return launch_bn<64, false>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s64, fault, st);
   }
-  return launch_bn<128>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s, fault, st);
+  if (args.subset == 0 && !args.lower) {
+    // A full rectangular update: tile pairs sharing their B rows (the jobs
+    // are the pairs; an odd last tile row pairs with rows beyond M, which
+    // the TMA fills with zeros and the epilogue does not write).
+    TGemmSched sp = s;
+    sp.tiles = ((s.m_tiles + 1) / 2) * s.n_tiles;
+    return launch_bn<128, true>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, sp, fault, st);
+  }
+  return launch_bn<128, false>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s, fault, st);
 }
 
 }  // namespace gptq

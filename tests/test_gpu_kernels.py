@@ -33,7 +33,10 @@ def split(x):
 
 @pytest.mark.parametrize("M,N,K,lower,row_off", [(128, 128, 128, 0, 0), (300, 200, 96, 0, 0),
                                                  (1000, 1100, 128, 1, 100), (4096, 3968, 128, 0, 0),
-                                                 (256, 640, 40, 1, 384)])
+                                                 (256, 640, 40, 1, 384),
+                                                 # CTA pairs sharing B: an odd number of tile rows
+                                                 # (the last pair half beyond M), ragged N and K
+                                                 (1100, 2500, 96, 0, 0), (4096, 1536, 512, 0, 0)])
 def test_tgemm_3xtf32(lib, M, N, K, lower, row_off):
     import torch
     rng = np.random.Generator(np.random.PCG64(M + N + K))
