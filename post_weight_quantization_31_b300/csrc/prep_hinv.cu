@@ -176,7 +176,12 @@ __global__ void prep_gather_kernel(const float* __restrict__ S, const int32_t* _
 }
 
 // ---------------------------------------------------------------- panel step
-constexpr int PT = 512;   // threads per panel CTA
+constexpr int PT = 512;   // threads per role CTA
+// Threads of the factor CTA: its widest phases (the update of the diagonal
+// block after the first sub-panel, and the inverse's block-row sums after
+// the last) take 384 threads, and with 384 the factorization's registers
+// (up to 168 a thread) hold its 32-entry rows without spilling.
+constexpr int FT = 384;
 constexpr int LDM = NB + 4;  // padded row (16-byte aligned rows)
 
 struct PanelArgs {
@@ -317,7 +322,7 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
   const int nsub = b >> 5;
   // The lower 4-wide chunks of the block (zero elsewhere), all copies in
   // flight at once; then the diagonal gets its low part, hi + lo.
-  for (int q = t; q < NB * (NB / 4); q += PT) {
+  for (int q = t; q < NB * (NB / 4); q += FT) {
     const int i = q / (NB / 4), c4 = (q % (NB / 4)) * 4;
     const bool ok = i < b && c4 <= i;
     cp_async16(Ls + i * LDM + c4, ok ? Z + static_cast<int64_t>(k + i) * ldz + k + c4 : Z, ok);
@@ -330,10 +335,12 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
   bool bad = false;
   for (int s = 0; s < nsub; ++s) {
     const int c0 = 32 * s;
-    if (warp > 0 && s >= 2 && t - 32 < (s - 1) * 128) {
-      // block row s - 1 of M, second half, beside the factorization
-      inverse_rows_finish(s - 1, (t - 32) >> 7, (t - 32) & 127, Tm, Mt);
-    }
+    // block row s - 1 of M, second half, beside the factorization, on the
+    // warps that do not share a scheduler with the factoring warp 0
+    // (warp w goes to scheduler w mod 4): warps 1-3, 5-7, 9-11 in order.
+    const int gf = 32 * (warp - warp / 4 - 1) + lane;
+    if ((warp & 3) != 0 && s >= 2 && gf < (s - 1) * 128)
+      inverse_rows_finish(s - 1, gf >> 7, gf & 127, Tm, Mt);
     if (warp == 0) {
       // ---- F: Cholesky of the diagonal sub-block, lane = row
       float a[32];
@@ -350,14 +357,15 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
       for (int c = 0; c < 32; ++c)
         if (c > lane) a[c] = 0.f;
       float my_r = 1.f;
+      float mypiv = 1.f;  // this lane's pivot (checked after the loop)
       float pn = a[0];  // lane j's current diagonal when column j starts
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float ajj = __shfl_sync(0xffffffffu, pn, j);
-        if (!(ajj > 0.f)) {
-          bad = true;
-          ajj = 1.f;
-        }
+        // A pivot that is not positive is replaced by 1 and reported below;
+        // no branch in the loop (a branch here made the loop spill).
+        if (lane == j) mypiv = ajj;
+        ajj = ajj > 0.f ? ajj : 1.f;
         const float r = rsqrtf(ajj);  // 1 / l_jj
         if (lane == j) my_r = r;
         const float l = (lane == j) ? ajj * r : a[j] * r;  // l_ij for lanes i >= j
@@ -384,13 +392,14 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
             make_float4(c <= lane ? a[c] : 0.f, c + 1 <= lane ? a[c + 1] : 0.f,
                         c + 2 <= lane ? a[c + 2] : 0.f, c + 3 <= lane ? a[c + 3] : 0.f);
       rdiag[c0 + lane] = my_r;
+      if (__any_sync(0xffffffffu, !(mypiv > 0.f))) bad = true;
 #pragma unroll
       for (int c = 0; c < 32; ++c) LssT[c * LST + lane] = (c <= lane) ? a[c] : 0.f;
     }
     __syncthreads();
     // ---- T: rows below the sub-block, within the diagonal block (at most
     //      three warps), and the inverse of the diagonal sub-block (last warp)
-    if (warp == PT / 32 - 1) invert_diag_block(s, Ls, rdiag, Mt, lane);
+    if (warp == FT / 32 - 1) invert_diag_block(s, Ls, rdiag, Mt, lane);
     if (t < b - c0 - 32) {
       float* row = Ls + (c0 + 32 + t) * LDM + c0;
       float a[32];
@@ -579,7 +588,7 @@ __device__ __forceinline__ void role_products(const PanelArgs& p, bool xrole, in
 // The factorization is the step's sequential chain, so it runs alone on one
 // SM and writes only what the next kernel needs; the rest of the GPU stays
 // free for the update GEMM of the previous step.
-__global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
+__global__ void __launch_bounds__(FT, 1) panel_factor_kernel(PanelArgs p) {
   extern __shared__ __align__(16) float sm[];
   float* Mt = sm;                    // [NB][LDM]  (L_kk^-1)^T
   float* Ls = Mt + NB * LDM;         // [NB][LDM]  diagonal block, then L_kk
@@ -589,7 +598,7 @@ __global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
   float* colbuf = Tm + 3 * 32 * TMLD;  // [2][32]
   float* LssT = colbuf + 64;         // [32][LST] transposed diagonal sub-block
   const int t = threadIdx.x;
-  for (int q = t; q < NB * (NB / 4); q += PT)
+  for (int q = t; q < NB * (NB / 4); q += FT)
     *reinterpret_cast<float4*>(Mt + (q / (NB / 4)) * LDM + (q % (NB / 4)) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   // Launched with programmatic dependent launch.  The diagonal block comes
   // from the priority GEMM, which has completed once the kernel before this
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(PT, 1) panel_factor_kernel(PanelArgs p) {
   const bool notpd = factor_invert_blocked(p.Z, p.zlo, p.n, p.k, p.b, Mt, Ls, rdiag, Tm, LT, colbuf, LssT);
   if (t == 0 && notpd) atomicOr(p.status, kStatNotPD);
   __syncthreads();
-  for (int idx = t; idx < NB * (NB / 4); idx += PT) {
+  for (int idx = t; idx < NB * (NB / 4); idx += FT) {
     const int c = idx / (NB / 4), r4 = (idx % (NB / 4)) * 4;
     *reinterpret_cast<float4*>(p.Mg + c * NB + r4) = *reinterpret_cast<const float4*>(Mt + c * LDM + r4);
   }
@@ -794,7 +803,7 @@ gptq_status_t launch_prepare(const float* S, const double* diag, int64_t d64, in
     const int tiles = pa.n_acc + n_pan;
     pa.split = (4 * tiles < sms) ? 4 : (2 * tiles < sms) ? 2 : 1;
     count_launch();
-    if (cudaSuccess != launch_pdl(panel_factor_kernel, dim3(1), dim3(PT), smem_factor, st, pa) ||
+    if (cudaSuccess != launch_pdl(panel_factor_kernel, dim3(1), dim3(FT), smem_factor, st, pa) ||
         cudaSuccess != cudaGetLastError()) {
       result = GPTQ_ERR_CUDA;
       break;
