@@ -72,7 +72,7 @@ __host__ __device__ __forceinline__ int subset_row_tiles(const TGemmArgs& a, int
 
 // The t-th tile of the subset, rows in order, columns in order within a row.
 template <int BN>
-__device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
+__host__ __device__ __forceinline__ void tile_coords(const TGemmArgs& a, const TGemmSched& s, int t, int& mt,
                                             int& nt) {
   for (mt = 0; mt < s.m_tiles; ++mt) {
     const int c = subset_row_tiles<BN>(a, s.n_tiles, mt);
@@ -463,6 +463,35 @@ gptq_status_t launch_bn(const float* A_hi, const float* A_lo, int64_t lda, const
 
 int tgemm_tile_count(const TGemmArgs& args) { return make_sched<128>(args).tiles; }
 
+// A launch that would fill fewer than half the SMs with 128 x 128 tiles runs
+// 128 x 64 tiles: twice the CTAs, each tile's loads, MMAs and epilogue about
+// half.
+static bool narrow_tiles(int tiles128, int sms) { return 2 * tiles128 <= sms; }
+
+// The tiles of one launch for a GPU with `sms` SMs, in the order its CTAs
+// take them (tile row, tile column); returns the count and the tile width.
+template <int BN>
+static int list_tiles(const TGemmArgs& a, int32_t* coords, int cap) {
+  const TGemmSched s = make_sched<BN>(a);
+  for (int t = 0; t < s.tiles && t < cap; ++t) {
+    int mt, nt;
+    tile_coords<BN>(a, s, t, mt, nt);
+    coords[2 * t] = mt;
+    coords[2 * t + 1] = nt;
+  }
+  return s.tiles;
+}
+
+int tgemm_plan(const TGemmArgs& a, int sms, int* bn, int32_t* coords, int cap) {
+  const TGemmSched s = make_sched<128>(a);
+  if (s.tiles > 0 && narrow_tiles(s.tiles, sms)) {
+    *bn = 64;
+    return list_tiles<64>(a, coords, cap);
+  }
+  *bn = 128;
+  return list_tiles<128>(a, coords, cap);
+}
+
 gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t lda, const float* B_hi,
                                   const float* B_lo, int64_t ldb, const TGemmArgs& args, int* fault,
                                   cudaStream_t st) {
@@ -470,9 +499,7 @@ gptq_status_t launch_tgemm_3xtf32(const float* A_hi, const float* A_lo, int64_t 
   if (args.M <= 0 || args.N <= 0 || args.K <= 0) return GPTQ_OK;
   const TGemmSched s = make_sched<128>(args);
   if (s.tiles == 0) return GPTQ_OK;
-  // A launch that would fill fewer than half the SMs runs 128 x 64 tiles:
-  // twice the CTAs, each tile's loads, MMAs and epilogue about half.
-  if (2 * s.tiles <= sm_count()) {
+  if (narrow_tiles(s.tiles, sm_count())) {
     const TGemmSched s64 = make_sched<64>(args);
     return launch_bn<64, false>(A_hi, A_lo, lda, B_hi, B_lo, ldb, args, s64, fault, st);
   }
@@ -538,4 +565,29 @@ extern "C" GPTQ_API int gptq_internal_tgemm_subset(const float* A_hi, const floa
   if (tiles) *tiles = gptq::tgemm_tile_count(g);
   return gptq::launch_tgemm_3xtf32(A_hi, A_lo, lda, B_hi, B_lo, ldb, g, gptq::fault_word_ptr(),
                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Test hook (not part of the public header), host only: the tiles one update
+// launch of the given subset would take on a GPU with `sms` SMs, as (tile
+// row, tile column) pairs in the order the CTAs take them (at most cap
+// pairs written), and the tile width it would use (*bn: 64 or 128; tiles are
+// 128 rows high).  A full rectangular update runs the same 128 x 128 tiles
+// in vertically adjacent pairs.  Returns the tile count, or -1 for bad
+// arguments.  Nothing is launched.
+extern "C" GPTQ_API int gptq_internal_tgemm_tiles(int M, int N, int lower, int row_off, int col_off,
+                                                  int subset, int pri_nt, int sms, int* bn,
+                                                  int32_t* coords, int cap) {
+  if (M <= 0 || N <= 0 || subset < 0 || subset > 2 || pri_nt < 0 || sms <= 0 || !bn || cap < 0 ||
+      (cap > 0 && !coords))
+    return -1;
+  gptq::TGemmArgs g;
+  g.M = M;
+  g.N = N;
+  g.K = 128;
+  g.lower = lower;
+  g.row_off = row_off;
+  g.col_off = col_off;
+  g.subset = subset;
+  g.pri_nt = pri_nt;
+  return gptq::tgemm_plan(g, sms, bn, coords, cap);
 }
