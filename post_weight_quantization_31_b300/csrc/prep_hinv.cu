@@ -265,31 +265,43 @@ __device__ __forceinline__ void invert_diag_block(int s, const float* __restrict
   }
 }
 
-// First half of block (tb, sb) of M, sb < tb, by 128 threads (g in
-// [0, 128): row i = g % 32 of the block, columns 8 (g / 32) .. + 8):
-// R[i][c] = sum_{u=sb}^{tb-1} L_{tb,u} M_{u,sb}, into Tm slot sb.
+// First half of block (tb, sb) of M, sb < tb, by 64 threads (g in [0, 64):
+// rows i and i + 16 of the block with i = g % 16, columns 8 (g / 16) .. + 8):
+// R[i][c] = sum_{u=sb}^{tb-1} L_{tb,u} M_{u,sb}, into Tm slot sb.  Two rows
+// a thread, so that each column value read from shared memory feeds two
+// rows; every output is summed in the same order as with one row a thread.
 __device__ __forceinline__ void inverse_rows_sum(int tb, int sb, int g, const float* __restrict__ Ls,
                                                  const float* __restrict__ Mt, float* __restrict__ Tm) {
-  const int i = g & 31, cg8 = (g >> 5) * 8;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int i = g & 15, cg8 = (g >> 4) * 8;
+  float acc[2][8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) acc[h][cc] = 0.f;
   for (int u = sb; u < tb; ++u) {
     const float* li = Ls + (32 * tb + i) * LDM + 32 * u;
 #pragma unroll 2
     for (int m = 0; m < 32; m += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(li + m);
+      const float4 x0 = *reinterpret_cast<const float4*>(li + m);
+      const float4 x1 = *reinterpret_cast<const float4*>(li + 16 * LDM + m);
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
         const float4 y = *reinterpret_cast<const float4*>(Mt + (32 * sb + cg8 + cc) * LDM + 32 * u + m);
-        acc[cc] = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc[cc]))));
+        acc[0][cc] = fmaf(x0.x, y.x, fmaf(x0.y, y.y, fmaf(x0.z, y.z, fmaf(x0.w, y.w, acc[0][cc]))));
+        acc[1][cc] = fmaf(x1.x, y.x, fmaf(x1.y, y.y, fmaf(x1.z, y.z, fmaf(x1.w, y.w, acc[1][cc]))));
       }
     }
   }
-  float* tm = Tm + (sb * 32 + i) * TMLD + cg8;
-  *reinterpret_cast<float4*>(tm) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  *reinterpret_cast<float4*>(tm + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float* tm = Tm + (sb * 32 + i + 16 * h) * TMLD + cg8;
+    *reinterpret_cast<float4*>(tm) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+    *reinterpret_cast<float4*>(tm + 4) = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+  }
 }
 
-// Second half: M_{tb,sb} = -M_{tb,tb} R (same thread layout).
+// Second half, by 128 threads per sb (g in [0, 128): row i = g % 32,
+// columns 8 (g / 32) .. + 8): M_{tb,sb} = -M_{tb,tb} R.
 __device__ __forceinline__ void inverse_rows_finish(int tb, int sb, int g, const float* __restrict__ Tm,
                                                     float* __restrict__ Mt) {
   const int i = g & 31, cg8 = (g >> 5) * 8;
@@ -432,36 +444,38 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
       for (int c = 0; c < 32; ++c) LT[c * LDM + c0 + 32 + t] = a[c];
     }
     __syncthreads();
-    // ---- U: D_tu -= L_ts L_us^T for s < u <= t < nsub, 4 x 4 register tiles
-    //      with both operands read along rows of the transposed sub-panel LT
+    // ---- U: D_tu -= L_ts L_us^T for s < u <= t < nsub, 8 x 4 register tiles
+    //      (one warp a 32 x 32 block) with both operands read along rows of
+    //      the transposed sub-panel LT
     const int nt = nsub - s - 1;
     const int npairs = nt * (nt + 1) / 2;
-    if (t < npairs * 64) {
-      int pi = t >> 6;
+    if (t < npairs * 32) {
+      int pi = t >> 5;
       int tt = s + 1;
       while (pi > tt - s - 1) {  // pairs ordered (s+1,s+1), (s+2,s+1), (s+2,s+2), ...
         pi -= tt - s;
         ++tt;
       }
       const int uu = s + 1 + pi;
-      const int i0 = 32 * tt + 4 * ((t >> 3) & 7), j0 = 32 * uu + 4 * (t & 7);
-      float acc[4][4];
+      const int i0 = 32 * tt + 8 * ((t >> 3) & 3), j0 = 32 * uu + 4 * (t & 7);
+      float acc[8][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 8; ++r)
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
 #pragma unroll 8
       for (int m = 0; m < 32; ++m) {
-        const float4 x = *reinterpret_cast<const float4*>(LT + m * LDM + i0);
+        const float4 x0 = *reinterpret_cast<const float4*>(LT + m * LDM + i0);
+        const float4 x1 = *reinterpret_cast<const float4*>(LT + m * LDM + i0 + 4);
         const float4 y = *reinterpret_cast<const float4*>(LT + m * LDM + j0);
-        const float xv[4] = {x.x, x.y, x.z, x.w}, yv[4] = {y.x, y.y, y.z, y.w};
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w}, yv[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 8; ++r)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(xv[r], yv[c], acc[r][c]);
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 8; ++r) {
         float4* o = reinterpret_cast<float4*>(Ls + (i0 + r) * LDM + j0);
         float4 v = *o;
         v.x -= acc[r][0];
@@ -470,10 +484,10 @@ __device__ bool factor_invert_blocked(const float* __restrict__ Z, const float* 
         v.w -= acc[r][3];
         *o = v;
       }
-    } else if (s >= 1 && t - npairs * 64 < s * 128) {
+    } else if (s >= 1 && t - npairs * 32 < s * 64) {
       // block row s of M, first half, with the threads the update leaves idle
-      const int g = t - npairs * 64;
-      inverse_rows_sum(s, g >> 7, g & 127, Ls, Mt, Tm);
+      const int g = t - npairs * 32;
+      inverse_rows_sum(s, g >> 6, g & 63, Ls, Mt, Tm);
     }
     __syncthreads();
   }
