@@ -451,7 +451,15 @@ def quantize_layer_from_host(W_host: torch.Tensor, X_chunks, cfg: QuantConfig,
     solver.prepare()
     solver.quantize(W_dev)
     solver.pack()
-    solver.check()
     r = solver.result()
-    return {"qweight": r.qweight.to("cpu"), "qzeros": r.qzeros.to("cpu"),
-            "scales": r.scales.to("cpu"), "g_idx": r.g_idx.to("cpu")}
+    # The packed result goes to fresh pinned host tensors on the compute
+    # stream, behind the solve; check() then waits for that stream once and
+    # raises if the device reported an error.
+    out = {}
+    for name, t in (("qweight", r.qweight), ("qzeros", r.qzeros), ("scales", r.scales),
+                    ("g_idx", r.g_idx)):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t, non_blocking=True)
+        out[name] = h
+    solver.check()
+    return out
